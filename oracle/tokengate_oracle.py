@@ -1,0 +1,283 @@
+"""Plain, slow fp64 definitions of every step of TokenGate's gated prefill.
+
+TEST INFRASTRUCTURE ONLY -- used by the tests, the smoke check and the
+CPU-baseline timing; never by the product path.
+
+Sources (five web pages about one paper, "TokenGate: Adapting LLMs for Fast
+and Memory-Efficient Prefill with Learned Token Pruning"):
+
+[RU] telohudelo.online, "TokenGate ускоряет prefill в LLM до 11,3 раза за
+     счёт обучаемого отсева", section "Механизм token-gated attention".
+[TH] ai4bro.com, "Stanford เปิดตัว TokenGate เร่งความเร็ว Prefill ใน LLM
+     สูงสุด 11.3 เท่า", section "กลไกการทำงานของ Learned Token Pruning"
+     (three phases; token-gated attention; per-head gain and temperature).
+[DE] spke.com, "TokenGate – Token-Gated Attention macht das Vollfüllen von
+     langen Kontexten bis zu 11,3-mal schneller", sections "Wie hat TokenGate
+     das Pruning von Tokens verstanden?" and "Was ist token-gated Attention?".
+[IT] ai.info, "TokenGate riporta un prefill fino a 11,3 volte più veloce sui
+     contesti lunghi", section "TokenGate impara quali token mantenere".
+
+What the pages state: below gate layer L every token is processed; at L a
+small MLP scores each token from its post-attention residual and a top-K
+selector keeps the best-scoring document tokens ([DE], [TH] phase 2); the
+question part of the prompt is never pruned ([DE], [TH] phase 3); only the
+kept rows go up ([IT]); the layers above build no KV for pruned tokens
+([DE]); each kept token's score becomes a bias on the attention logits above
+the gate, MoE-router style, with a learnable per-head gain and a learnable
+temperature ([TH], [DE] "Was ist token-gated Attention?", [RU]).
+
+What they leave open, and the reading taken here (one line each):
+
+* logit form: l_ij = t * (q_i . k_j) / sqrt(dh) + g_h * log(sigmoid(s_j)),
+  causal on original positions, GQA with kv head = h // (Hq / Hkv).
+* gate MLP: s = w2 . GELU(W1 x + b1) + b2, GELU the exact erf form.
+* selection order: fp32 score bits mapped to a total order (-0 < +0, ties go
+  to the lower index); K counts document tokens only; output ascending.
+* every kept key gets the bias, query tokens included (the MLP scores every
+  token).
+* a pruned layer of the stack: x <- x + attn(qkv(RMSNorm(x))) (no RoPE, no
+  o-proj, no MLP).
+
+Everything runs in float64 on values widened exactly from their stored
+formats.  numpy's matmul, sort and erf are used as library primitives; there
+is no blocking or fusion beyond processing independent query rows in chunks.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf as _erf
+
+__all__ = [
+    "bf16_bits_to_f64", "f32_to_f64", "gelu_erf", "gate_score",
+    "score_key", "select_topk", "select_topk_by_rank", "SelectNaNError",
+    "logsigmoid", "gather_rows", "rmsnorm", "qkv_proj", "split_qkv",
+    "keybias_attn", "gated_layer", "pruned_stack",
+]
+
+
+# --------------------------------------------------------------------------
+# storage formats -> float64 (exact widening)
+# --------------------------------------------------------------------------
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 is the top half of an fp32 pattern; widening is exact."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def f32_to_f64(a: np.ndarray) -> np.ndarray:
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+def _widen(a: np.ndarray) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# phase 2a: the gate MLP  ([DE] "Wie hat TokenGate ...", Gate-Modul; [TH] phase 2)
+# --------------------------------------------------------------------------
+def gelu_erf(z: np.ndarray) -> np.ndarray:
+    """GELU(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2))."""
+    return 0.5 * z * (1.0 + _erf(z / math.sqrt(2.0)))
+
+
+def gate_score(X, W1, b1, w2, b2) -> np.ndarray:
+    """Score of every token from its residual row at the gate layer:
+    z = W1 x_i + b1 ; h = GELU(z) ; s_i = w2 . h + b2.
+
+    X [N][d], W1 [Hg][d] (bf16 bits or fp32), b1 [Hg] or None, w2 [Hg], b2.
+    Returns s [N] in float64."""
+    x = _widen(X)
+    W = _widen(W1)
+    z = x @ W.T
+    if b1 is not None:
+        z = z + _widen(b1)[None, :]
+    h = gelu_erf(z)
+    return h @ _widen(w2) + float(b2)
+
+
+# --------------------------------------------------------------------------
+# phase 2b: top-K over the document span, question never pruned
+#   ([DE] "Wie hat TokenGate ..."; [TH] phase 2 and 3; [IT])
+# --------------------------------------------------------------------------
+class SelectNaNError(ValueError):
+    """A NaN score inside the document span has no place in the order."""
+
+
+def score_key(scores_f32: np.ndarray) -> np.ndarray:
+    """Map fp32 score bits to uint32 keys whose unsigned order is the total
+    order used for selection: negative patterns are bit-inverted, the rest
+    get the sign bit set.  So -inf < ... < -0.0 < +0.0 < ... < +inf."""
+    u = np.ascontiguousarray(scores_f32, dtype=np.float32).view(np.uint32)
+    neg = (u & np.uint32(0x80000000)) != 0
+    return np.where(neg, ~u, u | np.uint32(0x80000000)).astype(np.uint32)
+
+
+def select_topk(scores_f32, doc_begin: int, doc_end: int, K: int) -> np.ndarray:
+    """Indices kept at the gate: every token outside [doc_begin, doc_end)
+    plus the K document tokens ranked first by (key descending, index
+    ascending); returned ascending as int64.  Raises SelectNaNError when a
+    document score is NaN."""
+    s = np.asarray(scores_f32, dtype=np.float32)
+    N = s.shape[0]
+    if not (0 <= doc_begin <= doc_end <= N) or not (0 <= K <= doc_end - doc_begin):
+        raise ValueError("bad span or K")
+    doc = s[doc_begin:doc_end]
+    if np.isnan(doc).any():
+        raise SelectNaNError("NaN score in the document span")
+    keys = score_key(doc).astype(np.int64)
+    pos = np.arange(doc_begin, doc_end, dtype=np.int64)
+    # lexsort: last key is primary -> sort by key descending, then index ascending
+    order = np.lexsort((pos, -keys))
+    kept_doc = np.sort(pos[order[:K]])
+    outside = np.concatenate([np.arange(0, doc_begin), np.arange(doc_end, N)]).astype(np.int64)
+    return np.sort(np.concatenate([outside, kept_doc]))
+
+
+def select_topk_by_rank(scores_f32, doc_begin: int, doc_end: int, K: int) -> np.ndarray:
+    """Second, independent definition for small inputs (pure Python): a
+    document token j is kept iff fewer than K document tokens beat it, where
+    i beats j when key_i > key_j, or key_i == key_j and i < j."""
+    s = [float(v) for v in np.asarray(scores_f32, dtype=np.float32)]
+    keys = [int(k) for k in score_key(np.asarray(scores_f32, dtype=np.float32))]
+    N = len(s)
+    out = []
+    for j in range(N):
+        if j < doc_begin or j >= doc_end:
+            out.append(j)
+            continue
+        if math.isnan(s[j]):
+            raise SelectNaNError("NaN score in the document span")
+        beats = 0
+        for i in range(doc_begin, doc_end):
+            if keys[i] > keys[j] or (keys[i] == keys[j] and i < j):
+                beats += 1
+        if beats < K:
+            out.append(j)
+    return np.asarray(out, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# phase 3 entry: gather the kept rows and their bias input
+#   ([IT] only the kept representations go up; [DE] "Was ist token-gated
+#   Attention?": the kept token's score becomes the bias)
+# --------------------------------------------------------------------------
+def logsigmoid(s) -> np.ndarray:
+    """log(sigmoid(s)) = min(s, 0) - log1p(exp(-|s|)), in float64."""
+    s = np.asarray(s, dtype=np.float64)
+    return np.minimum(s, 0.0) - np.log1p(np.exp(-np.abs(s)))
+
+
+def gather_rows(X, idx, scores_f32=None):
+    """Y[m] = X[idx[m]] (an exact copy, same storage format) and, when scores
+    are given, ls[m] = log(sigmoid(s[idx[m]])) in float64."""
+    X = np.asarray(X)
+    idx = np.asarray(idx, dtype=np.int64)
+    Y = X[idx].copy()
+    ls = None
+    if scores_f32 is not None:
+        ls = logsigmoid(np.asarray(scores_f32, dtype=np.float32).astype(np.float64)[idx])
+    return Y, ls
+
+
+# --------------------------------------------------------------------------
+# phase 3: the pruned layers ([DE] "Prune-Front-Behandlung"; [TH] phase 3)
+# --------------------------------------------------------------------------
+def rmsnorm(x, gamma, eps: float) -> np.ndarray:
+    """RMSNorm(x) = x * gamma / sqrt(mean(x^2) + eps), row-wise."""
+    x = _widen(x)
+    ms = np.mean(x * x, axis=1, keepdims=True)
+    return x * _widen(gamma)[None, :] / np.sqrt(ms + float(eps))
+
+
+def qkv_proj(X, Wqkv) -> np.ndarray:
+    """QKV = X Wqkv^T with Wqkv [(Hq + 2 Hkv) dh][d] (nn.Linear layout)."""
+    return _widen(X) @ _widen(Wqkv).T
+
+
+def split_qkv(QKV, Hq: int, Hkv: int, dh: int):
+    """Column blocks of the packed rows: q heads, then k heads, then v heads."""
+    q = QKV[:, : Hq * dh]
+    k = QKV[:, Hq * dh: (Hq + Hkv) * dh]
+    v = QKV[:, (Hq + Hkv) * dh: (Hq + 2 * Hkv) * dh]
+    return q, k, v
+
+
+def keybias_attn(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain, temperature: float,
+                 rows=None, return_rowsum: bool = False, chunk: int = 512):
+    """Token-gated causal attention over the kept rows.
+
+    For query head h (kv head h // (Hq / Hkv)) and kept row i:
+        l_ij = t * (q_i . k_j) / sqrt(dh) + g_h * ls_j   for j <= i
+        o_i  = sum_j softmax_j(l_ij) v_j
+    ``logsig_kept`` None drops the bias term (full prefill).  The causal
+    mask on compacted rows equals the mask on original positions because the
+    kept indices ascend.  ``rows`` (optional) restricts the output to those
+    query rows; the result is then [len(rows)][Hq dh].
+    Returns O (float64), and the largest |row sum of p - 1| if asked."""
+    Q = _widen(QKV)
+    M = Q.shape[0]
+    assert Hq % Hkv == 0, "GQA needs Hq divisible by Hkv"
+    G = Hq // Hkv
+    q_all, k_all, v_all = split_qkv(Q, Hq, Hkv, dh)
+    ls = None if logsig_kept is None else np.asarray(logsig_kept, dtype=np.float64)
+    g = np.asarray(gain, dtype=np.float64)
+    t = float(temperature)
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    O = np.zeros((rows.shape[0], Hq * dh), dtype=np.float64)
+    worst_rowsum = 0.0
+    for h in range(Hq):
+        hk = h // G
+        q = q_all[:, h * dh:(h + 1) * dh]
+        k = k_all[:, hk * dh:(hk + 1) * dh]
+        v = v_all[:, hk * dh:(hk + 1) * dh]
+        for c0 in range(0, rows.shape[0], chunk):
+            r = rows[c0:c0 + chunk]
+            jmax = int(r.max()) + 1
+            logits = t * (q[r] @ k[:jmax].T) / math.sqrt(dh)
+            if ls is not None:
+                logits = logits + g[h] * ls[None, :jmax]
+            causal = np.arange(jmax)[None, :] <= r[:, None]
+            logits = np.where(causal, logits, -np.inf)
+            mx = logits.max(axis=1, keepdims=True)
+            p = np.exp(logits - mx)
+            p = p / p.sum(axis=1, keepdims=True)
+            if return_rowsum:
+                worst_rowsum = max(worst_rowsum, float(np.abs(p.sum(axis=1) - 1.0).max()))
+            O[c0:c0 + chunk, h * dh:(h + 1) * dh] = p @ v[:jmax]
+    if return_rowsum:
+        return O, worst_rowsum
+    return O
+
+
+def gated_layer(X, W1, b1, w2, b2, doc_begin, doc_end, K, Wqkv, Hq, Hkv, dh, gain,
+                temperature, scores_f32=None):
+    """One gated layer end to end: score, select, gather, project, attend.
+
+    Selection is decided on fp32 scores (the format the selector reads); by
+    default the oracle's own scores rounded to fp32."""
+    s = gate_score(X, W1, b1, w2, b2)
+    s32 = s.astype(np.float32) if scores_f32 is None else np.asarray(scores_f32, np.float32)
+    idx = select_topk(s32, doc_begin, doc_end, K)
+    Xk, ls = gather_rows(X, idx, s32)
+    QKV = qkv_proj(Xk, Wqkv)
+    O = keybias_attn(QKV, Hq, Hkv, dh, ls, gain, temperature)
+    return {"scores": s, "idx": idx, "Xk": Xk, "logsig": ls, "QKV": QKV, "O": O}
+
+
+def pruned_stack(x0, layers, Hq, Hkv, dh, logsig_kept, eps: float = 1e-6):
+    """The layers above the gate on the kept rows:
+    x <- x + keybias_attn(qkv_proj(RMSNorm(x))) for each layer.
+    ``layers`` is a list of dicts with Wqkv, gamma, gain, temperature.
+    ``logsig_kept`` None runs the same layers as full prefill (no bias)."""
+    x = _widen(x0)
+    assert x.shape[1] == Hq * dh, "the residual add needs Hq * dh == d_model"
+    for L in layers:
+        xn = rmsnorm(x, L["gamma"], eps)
+        qkv = qkv_proj(xn, L["Wqkv"])
+        x = x + keybias_attn(qkv, Hq, Hkv, dh, logsig_kept, L["gain"], L["temperature"])
+    return x

@@ -1,0 +1,403 @@
+"""Pins for the fp64 oracle: each check ties it to something other than
+itself -- a closed form, a library routine computing a special case (or the
+same definition by a different code path), a brute-force definition on tiny
+inputs, or a hand-worked fixture.  CPU only."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+from scipy.stats import norm
+
+import oracle as O
+import tg_inputs as TI
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+torch.set_num_threads(min(8, os.cpu_count() or 1))
+
+
+# ------------------------------------------------------------------ gate ---
+def test_gelu_matches_normal_cdf_and_torch():
+    z = np.linspace(-12, 12, 4001)
+    ref_cdf = z * norm.cdf(z)                          # z * Phi(z), scipy.stats
+    ref_torch = F.gelu(torch.from_numpy(z), approximate="none").numpy()
+    got = O.gelu_erf(z)
+    np.testing.assert_allclose(got, ref_cdf, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(got, ref_torch, rtol=1e-13, atol=1e-15)
+    assert O.gelu_erf(np.array([0.0]))[0] == 0.0
+    assert abs(O.gelu_erf(np.array([30.0]))[0] - 30.0) < 1e-12       # ~identity
+    assert abs(O.gelu_erf(np.array([-30.0]))[0]) < 1e-150            # ~zero
+
+
+def test_gate_score_matches_torch_mlp():
+    rng = np.random.default_rng(1)
+    N, d, Hg = 37, 24, 10                       # non-square so a transpose fails
+    X = rng.standard_normal((N, d)).astype(np.float32)
+    W1 = rng.standard_normal((Hg, d)).astype(np.float32) / 5
+    b1 = rng.standard_normal(Hg).astype(np.float32)
+    w2 = rng.standard_normal(Hg).astype(np.float32)
+    b2 = 0.375
+    lin1 = torch.nn.Linear(d, Hg).double()
+    lin2 = torch.nn.Linear(Hg, 1).double()
+    with torch.no_grad():
+        lin1.weight.copy_(torch.from_numpy(W1.astype(np.float64)))
+        lin1.bias.copy_(torch.from_numpy(b1.astype(np.float64)))
+        lin2.weight.copy_(torch.from_numpy(w2.astype(np.float64))[None, :])
+        lin2.bias.fill_(b2)
+        ref = lin2(F.gelu(lin1(torch.from_numpy(X.astype(np.float64))))).squeeze(1).numpy()
+    got = O.gate_score(X, W1, b1, w2, b2)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gate_score_zero_weight_is_constant():
+    rng = np.random.default_rng(2)
+    N, d, Hg = 9, 16, 8
+    X = rng.standard_normal((N, d)).astype(np.float32)
+    b1 = rng.standard_normal(Hg).astype(np.float32)
+    w2 = rng.standard_normal(Hg).astype(np.float32)
+    got = O.gate_score(X, np.zeros((Hg, d), np.float32), b1, w2, -1.5)
+    # W1 = 0: every token scores w2 . GELU(b1) + b2, with GELU = z Phi(z)
+    const = float(np.dot(w2.astype(np.float64), b1 * norm.cdf(b1.astype(np.float64)))) - 1.5
+    np.testing.assert_allclose(got, np.full(N, const), rtol=1e-13)
+
+
+def test_gate_score_reads_bf16_bits_exactly():
+    w = TI.Workload("t", N=8, doc_begin=0, doc_end=8, d=32, Hg=16, Hq=2, Hkv=1, dh=16,
+                    dtype="bf16", seed=5)
+    X = TI.residual(w)
+    gp = TI.gate_params(w, gate_biases=True)
+    # widening bf16 bits must equal torch's own bf16 -> f64 conversion
+    xt = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(O.bf16_bits_to_f64(X), xt)
+    Wt = torch.from_numpy(gp["W1"].view(np.int16)).view(torch.bfloat16).double()
+    ref = (F.gelu(torch.from_numpy(xt) @ Wt.T + torch.from_numpy(gp["b1"].astype(np.float64)))
+           @ torch.from_numpy(gp["w2"].astype(np.float64)) + gp["b2"]).numpy()
+    np.testing.assert_allclose(O.gate_score(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"]), ref,
+                               rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- select ---
+def test_score_key_total_order():
+    vals = np.array([-np.inf, -3.0, -1e-40, -0.0, 0.0, 1e-40, 2.0, np.inf], dtype=np.float32)
+    keys = O.score_key(vals)
+    assert list(np.argsort(keys, kind="stable")) == list(range(len(vals)))
+    assert len(set(keys.tolist())) == len(vals)          # -0 and +0 differ
+    rng = np.random.default_rng(3)
+    a = rng.standard_normal(5000).astype(np.float32) * 10
+    b = rng.standard_normal(5000).astype(np.float32) * 10
+    ka, kb = O.score_key(a), O.score_key(b)
+    # for distinct finite values the key order is the float order
+    ne = a != b
+    assert np.array_equal((ka > kb)[ne], (a > b)[ne])
+
+
+def _read_golden_select():
+    data = {}
+    with open(os.path.join(GOLDEN, "select_worked_example.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            if line.startswith("K "):
+                k, rest = line[2:].split(":")
+                data.setdefault("cases", []).append((int(k), [int(v) for v in rest.split()]))
+            else:
+                key, *vals = line.split()
+                data[key] = vals
+    return data
+
+
+def test_select_hand_worked_fixture():
+    g = _read_golden_select()
+    s = np.array([float(v) for v in g["scores"]], dtype=np.float32)
+    b, e = int(g["doc_begin"][0]), int(g["doc_end"][0])
+    assert s.shape[0] == int(g["N"][0])
+    assert np.signbit(s[3]) and not np.signbit(s[6])
+    for K, expect in g["cases"]:
+        assert O.select_topk(s, b, e, K).tolist() == expect, K
+        assert O.select_topk_by_rank(s, b, e, K).tolist() == expect, K
+
+
+def test_select_sort_equals_rank_definition_exhaustive_small():
+    values = np.array([-np.inf, -1.0, -0.0, 0.0, 1.0, np.inf], dtype=np.float32)
+    n = 4
+    for combo in itertools.product(range(len(values)), repeat=n):
+        s = values[list(combo)]
+        for b, e in ((0, 4), (1, 3), (0, 2), (2, 4), (1, 1)):
+            for K in range(0, e - b + 1):
+                assert np.array_equal(O.select_topk(s, b, e, K),
+                                      O.select_topk_by_rank(s, b, e, K)), (s, b, e, K)
+
+
+def test_select_sort_equals_rank_definition_random():
+    rng = np.random.default_rng(4)
+    for trial in range(300):
+        n = int(rng.integers(1, 40))
+        pool = np.array([-np.inf, -2.5, -0.0, 0.0, 1e-42, 0.5, 0.5, 3.0, np.inf], np.float32)
+        s = pool[rng.integers(0, len(pool), size=n)] if trial % 2 else \
+            rng.standard_normal(n).astype(np.float32)
+        b = int(rng.integers(0, n + 1))
+        e = int(rng.integers(b, n + 1))
+        K = int(rng.integers(0, e - b + 1))
+        assert np.array_equal(O.select_topk(s, b, e, K), O.select_topk_by_rank(s, b, e, K))
+
+
+@pytest.mark.parametrize("kind", TI.ADVERSARIAL_KINDS)
+def test_select_invariants(kind):
+    N, b, e = 3000, 100, 2800
+    s = TI.adversarial_scores(kind, N, seed=7)
+    keys = O.score_key(s)
+    for K in (0, 1, 17, 1350, e - b - 1, e - b):
+        idx = O.select_topk(s, b, e, K)
+        assert idx.shape[0] == N - (e - b) + K
+        assert np.all(np.diff(idx) > 0)                       # strictly ascending
+        outside = np.r_[0:b, e:N]
+        assert np.isin(outside, idx).all()                    # question never pruned
+        kept = idx[(idx >= b) & (idx < e)]
+        dropped = np.setdiff1d(np.arange(b, e), kept)
+        if kept.size and dropped.size:                        # no dropped token beats a kept one
+            kk, kd = keys[kept], keys[dropped]
+            assert kd.max() <= kk.min()
+            tie = keys[kept].min()
+            if (kd == tie).any():                             # ties resolved by lower index
+                assert kept[keys[kept] == tie].max() < dropped[kd == tie].min()
+    if kind == "all_equal":
+        assert np.array_equal(O.select_topk(s, b, e, 5)[b:b + 5], np.arange(b, b + 5))
+
+
+def test_select_nan_is_error_only_inside_span():
+    s = np.zeros(10, np.float32)
+    s[7] = np.nan
+    with pytest.raises(O.SelectNaNError):
+        O.select_topk(s, 2, 9, 3)
+    assert O.select_topk(s, 0, 5, 2).tolist() == [0, 1, 5, 6, 7, 8, 9]
+
+
+# --------------------------------------------------------------- gather ---
+def test_logsigmoid_closed_forms_and_torch():
+    assert O.logsigmoid(0.0) == pytest.approx(-math.log(2.0), rel=1e-15)
+    s = np.linspace(-60, 60, 2401)
+    np.testing.assert_allclose(O.logsigmoid(s) - O.logsigmoid(-s), s, atol=1e-12)
+    ref = F.logsigmoid(torch.from_numpy(s)).numpy()
+    np.testing.assert_allclose(O.logsigmoid(s), ref, rtol=1e-14, atol=1e-300)
+    # asymptotes, no overflow
+    assert O.logsigmoid(-100.0) == pytest.approx(-100.0, rel=1e-15)
+    assert O.logsigmoid(100.0) == pytest.approx(-math.exp(-100.0), rel=1e-12)
+    assert O.logsigmoid(30.0) == pytest.approx(-math.exp(-30.0), rel=1e-12)
+    assert O.logsigmoid(-30.0) == pytest.approx(-30.0 - math.exp(-30.0), rel=1e-15)
+    assert O.logsigmoid(-1000.0) == -1000.0 and O.logsigmoid(1000.0) == 0.0
+
+
+def test_gather_identity_and_copy():
+    rng = np.random.default_rng(5)
+    X = TI.f32_to_bf16_bits(rng.standard_normal((50, 16)).astype(np.float32))
+    s = rng.standard_normal(50).astype(np.float32)
+    Y, ls = O.gather_rows(X, np.arange(50), s)
+    assert np.array_equal(Y, X)
+    idx = np.array([0, 3, 4, 49])
+    Y, ls = O.gather_rows(X, idx, s)
+    for m, i in enumerate(idx):
+        assert np.array_equal(Y[m], X[i])
+    ref = F.logsigmoid(torch.from_numpy(s.astype(np.float64)[idx])).numpy()
+    np.testing.assert_allclose(ls, ref, rtol=1e-14)
+
+
+# ----------------------------------------------------------- projection ---
+def test_rmsnorm_matches_torch_and_invariants():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((20, 48)).astype(np.float32) * 3
+    gm = rng.uniform(0.9, 1.1, 48).astype(np.float32)
+    ref = F.rms_norm(torch.from_numpy(x.astype(np.float64)), (48,),
+                     weight=torch.from_numpy(gm.astype(np.float64)), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rmsnorm(x, gm, 1e-6), ref, rtol=1e-13)
+    y = O.rmsnorm(x, np.ones(48, np.float32), 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-13)     # unit RMS
+    np.testing.assert_allclose(O.rmsnorm(x * np.float32(4), gm, 0.0), O.rmsnorm(x, gm, 0.0),
+                               rtol=1e-13)                                  # scale-free
+
+
+def test_qkv_proj_identity_brute_force_and_torch():
+    rng = np.random.default_rng(7)
+    M, d, cols = 5, 6, 10
+    X = rng.standard_normal((M, d)).astype(np.float32)
+    W = rng.standard_normal((cols, d)).astype(np.float32)
+    got = O.qkv_proj(X, W)
+    for i in range(M):                       # brute-force triple loop
+        for j in range(cols):
+            acc = 0.0
+            for c in range(d):
+                acc += float(X[i, c]) * float(W[j, c])
+            assert got[i, j] == pytest.approx(acc, rel=1e-12, abs=1e-12)
+    ref = F.linear(torch.from_numpy(X.astype(np.float64)), torch.from_numpy(W.astype(np.float64)))
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-13, atol=1e-13)
+    eye = np.zeros((cols, d), np.float32)
+    eye[:d, :d] = np.eye(d)
+    np.testing.assert_array_equal(O.qkv_proj(X, eye)[:, :d], X.astype(np.float64))
+    assert not O.qkv_proj(X, eye)[:, d:].any()
+
+
+# ------------------------------------------------------------ attention ---
+def _rand_qkv(M, Hq, Hkv, dh, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((M, (Hq + 2 * Hkv) * dh)) * scale
+
+
+def _sdpa(QKV, Hq, Hkv, dh, ls, g, t):
+    """torch SDPA in float64 with enable_gqa; the key bias g_h * ls_j and
+    the causal mask go in as an additive float mask."""
+    q, k, v = O.split_qkv(torch.from_numpy(QKV), Hq, Hkv, dh)
+    M = QKV.shape[0]
+    q = q.reshape(M, Hq, dh).transpose(0, 1)[None]
+    k = k.reshape(M, Hkv, dh).transpose(0, 1)[None]
+    v = v.reshape(M, Hkv, dh).transpose(0, 1)[None]
+    causal = torch.ones(M, M, dtype=torch.bool).tril()
+    if ls is None:
+        bias = torch.zeros(Hq, M, M, dtype=torch.float64)
+    else:
+        bias = torch.from_numpy(np.asarray(g, np.float64))[:, None, None] * \
+            torch.from_numpy(np.asarray(ls, np.float64))[None, None, :].expand(Hq, M, M)
+    mask = torch.where(causal[None], bias, torch.tensor(-math.inf, dtype=torch.float64))
+    out = F.scaled_dot_product_attention(q, k, v, attn_mask=mask[None], scale=t / math.sqrt(dh),
+                                         enable_gqa=True)
+    return out[0].transpose(0, 1).reshape(M, Hq * dh).numpy()
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (4, 4), (6, 2), (2, 1)])
+def test_attn_matches_sdpa_with_bias_mask(Hq, Hkv):
+    dh, M = 8, 37
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=Hq * 10 + Hkv)
+    rng = np.random.default_rng(11)
+    ls = -rng.exponential(1.0, M)
+    g = rng.uniform(0.5, 1.5, Hq)
+    got = O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, 1.1)
+    np.testing.assert_allclose(got, _sdpa(QKV, Hq, Hkv, dh, ls, g, 1.1), rtol=1e-11, atol=1e-12)
+
+
+def test_attn_g0_t1_is_textbook_causal_attention():
+    Hq, Hkv, dh, M = 4, 2, 16, 50
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=12)
+    q, k, v = O.split_qkv(torch.from_numpy(QKV), Hq, Hkv, dh)
+    q = q.reshape(M, Hq, dh).transpose(0, 1)[None]
+    k = k.reshape(M, Hkv, dh).transpose(0, 1)[None]
+    v = v.reshape(M, Hkv, dh).transpose(0, 1)[None]
+    ref = F.scaled_dot_product_attention(q, k, v, is_causal=True, enable_gqa=True)
+    ref = ref[0].transpose(0, 1).reshape(M, Hq * dh).numpy()
+    ls = -np.random.default_rng(0).exponential(1.0, M)
+    got = O.keybias_attn(QKV, Hq, Hkv, dh, ls, np.zeros(Hq), 1.0)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(O.keybias_attn(QKV, Hq, Hkv, dh, None, np.ones(Hq), 1.0), ref,
+                               rtol=1e-11, atol=1e-12)
+
+
+def test_attn_two_key_closed_form():
+    # row 1 sees keys 0 and 1: o_1 = v_0 + sigmoid(l_11 - l_10) (v_1 - v_0)
+    Hq, Hkv, dh = 2, 1, 4
+    QKV = _rand_qkv(2, Hq, Hkv, dh, seed=13)
+    ls = np.array([-0.3, -2.0])
+    g = np.array([0.7, 1.4])
+    t = 1.3
+    got = O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, t)
+    q, k, v = O.split_qkv(QKV, Hq, Hkv, dh)
+    for h in range(Hq):
+        qh = q[1, h * dh:(h + 1) * dh]
+        delta = t * (qh @ k[1] - qh @ k[0]) / math.sqrt(dh) + g[h] * (ls[1] - ls[0])
+        sig = 1.0 / (1.0 + math.exp(-delta))
+        np.testing.assert_allclose(got[1, h * dh:(h + 1) * dh], v[0] + sig * (v[1] - v[0]),
+                                   rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(got[0, h * dh:(h + 1) * dh], v[0], rtol=0, atol=1e-15)
+
+
+def test_attn_bias_invariances_and_rowsum():
+    Hq, Hkv, dh, M = 4, 2, 8, 33
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=14)
+    g = np.array([0.6, 0.9, 1.2, 1.5])
+    base = O.keybias_attn(QKV, Hq, Hkv, dh, None, g, 0.8)
+    same = O.keybias_attn(QKV, Hq, Hkv, dh, np.full(M, -1.7), g, 0.8)   # equal ls cancel
+    np.testing.assert_allclose(same, base, rtol=1e-12, atol=1e-13)
+    # temperature with g = 0 is a scale on q
+    Qs = QKV.copy()
+    Qs[:, :Hq * dh] *= 0.8
+    np.testing.assert_allclose(O.keybias_attn(Qs, Hq, Hkv, dh, None, g, 1.0), base,
+                               rtol=1e-12, atol=1e-13)
+    ls = -np.random.default_rng(1).exponential(1.0, M)
+    _, worst = O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, 0.8, return_rowsum=True)
+    assert worst < 1e-14
+    # a dominant bias on one key concentrates every later row on that key
+    ls2 = np.full(M, -60.0)
+    ls2[5] = 0.0
+    out = O.keybias_attn(QKV * 0.01, Hq, Hkv, dh, ls2, np.full(Hq, 1.0), 1.0)
+    _, _, v = O.split_qkv(QKV * 0.01, Hq, Hkv, dh)
+    for h in range(Hq):
+        hk = h // 2
+        np.testing.assert_allclose(out[5:, h * dh:(h + 1) * dh],
+                                   np.broadcast_to(v[5, hk * dh:(hk + 1) * dh], (M - 5, dh)),
+                                   rtol=1e-12, atol=1e-14)
+
+
+def test_attn_row_subset_matches_full():
+    Hq, Hkv, dh, M = 4, 2, 8, 70
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=15)
+    ls = -np.random.default_rng(2).exponential(1.0, M)
+    g = np.linspace(0.5, 1.5, Hq)
+    full = O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, 1.1, chunk=16)
+    rows = np.array([0, 1, 31, 32, 69])
+    np.testing.assert_allclose(O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, 1.1, rows=rows),
+                               full[rows], rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------- whole layer ---
+def test_gated_layer_keep_all_is_full_prefill():
+    w = TI.WORKLOADS["tiny_f32_n512"]
+    X = TI.residual(w)
+    gp = TI.gate_params(w)
+    Wqkv = TI.qkv_weight(w)
+    ap = TI.attn_params(w)
+    out = O.gated_layer(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"], w.doc_begin, w.doc_end, w.D,
+                        Wqkv, w.Hq, w.Hkv, w.dh, ap["gain"], ap["temperature"])
+    assert np.array_equal(out["idx"], np.arange(w.N))
+    full = O.keybias_attn(O.qkv_proj(X, Wqkv), w.Hq, w.Hkv, w.dh,
+                          O.logsigmoid(out["scores"].astype(np.float32).astype(np.float64)),
+                          ap["gain"], ap["temperature"])
+    np.testing.assert_allclose(out["O"], full, rtol=1e-12, atol=1e-13)
+    # and with g = 0, t = 1 it is plain causal attention of the full prompt
+    out0 = O.gated_layer(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"], w.doc_begin, w.doc_end, w.D,
+                         Wqkv, w.Hq, w.Hkv, w.dh, np.zeros(w.Hq), 1.0)
+    np.testing.assert_allclose(out0["O"], _sdpa(O.qkv_proj(X, Wqkv), w.Hq, w.Hkv, w.dh, None,
+                                                np.zeros(w.Hq), 1.0), rtol=1e-10, atol=1e-12)
+
+
+def test_gated_layer_query_rows_kept_and_attend_only_kept_keys():
+    w = TI.WORKLOADS["tiny_f32_n512"]
+    X = TI.residual(w)
+    gp = TI.gate_params(w)
+    Wqkv = TI.qkv_weight(w)
+    ap = TI.attn_params(w)
+    K = w.Ks()[0]
+    out = O.gated_layer(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"], w.doc_begin, w.doc_end, K,
+                        Wqkv, w.Hq, w.Hkv, w.dh, ap["gain"], ap["temperature"])
+    idx = out["idx"]
+    assert idx.shape[0] == w.M(K) == 192
+    assert np.array_equal(idx[-64:], np.arange(448, 512))
+    # pruned keys carry no KV: attention over the kept rows equals full
+    # attention in which every pruned key's logit is -inf
+    s32 = out["scores"].astype(np.float32)
+    QKVfull = O.qkv_proj(X, Wqkv)
+    ls_full = O.logsigmoid(s32.astype(np.float64)).copy()
+    pruned = np.setdiff1d(np.arange(w.N), idx)
+    ls_full_masked = ls_full.copy()
+    ls_full_masked[pruned] = -np.inf
+    full = O.keybias_attn(QKVfull, w.Hq, w.Hkv, w.dh, ls_full_masked, np.maximum(ap["gain"], 1e-3),
+                          ap["temperature"], rows=idx)
+    np.testing.assert_allclose(out["O"], full, rtol=1e-11, atol=1e-12)
+
+
+def test_pruned_stack_zero_layers_and_zero_weights():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((12, 16)).astype(np.float32)
+    assert np.array_equal(O.pruned_stack(x, [], 4, 2, 4, None), x.astype(np.float64))
+    L = {"Wqkv": np.zeros((32, 16), np.float32), "gamma": np.ones(16, np.float32),
+         "gain": np.ones(4), "temperature": 1.0}
+    np.testing.assert_array_equal(O.pruned_stack(x, [L, L], 4, 2, 4, None), x.astype(np.float64))
