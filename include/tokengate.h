@@ -1,0 +1,207 @@
+/*
+ * tokengate.h -- C ABI of libtokengate.so: the gated-prefill hot path of
+ * TokenGate-style learned token pruning, as hand-written CUDA for sm_103a.
+ *
+ * The method (five web pages about "TokenGate: Adapting LLMs for Fast and
+ * Memory-Efficient Prefill with Learned Token Pruning"):
+ *   [DE] spke.com, "TokenGate – Token-Gated Attention macht das Vollfüllen
+ *        von langen Kontexten bis zu 11,3-mal schneller", sections "Wie hat
+ *        TokenGate das Pruning von Tokens verstanden?" (three phases: full
+ *        layers below gate layer L, a gate MLP + top-K at L, pruned layers
+ *        above; only the document part may be pruned) and "Was ist
+ *        token-gated Attention?" (the kept token's score becomes a bias on
+ *        the attention logits, with a per-head gain and a temperature).
+ *   [TH] ai4bro.com, "Stanford เปิดตัว TokenGate เร่งความเร็ว Prefill ใน LLM
+ *        สูงสุด 11.3 เท่า", section "กลไกการทำงานของ Learned Token Pruning".
+ *   [IT] ai.info, "TokenGate riporta un prefill fino a 11,3 volte più veloce
+ *        sui contesti lunghi", section "TokenGate impara quali token
+ *        mantenere" (only the kept rows go to the upper layers).
+ * The pages give no formula; this library fixes the logit as
+ *   l_ij = t * (q_i . k_j) / sqrt(dh) + g_h * log(sigmoid(s_j)),
+ * causal on original positions, with grouped-query attention.
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers unless marked "host".  The caller owns all
+ *    buffers; the library allocates no device memory on any call.
+ *  - Matrices are row-major with densely packed rows.  bf16 buffers hold
+ *    IEEE bfloat16; fp32 buffers IEEE binary32.  Every device pointer must
+ *    be 16-byte aligned, and every row's byte length a multiple of 16.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and never synchronise, except tg_get_device_status.
+ *  - Argument errors (NULL pointers, misalignment, sizes out of range,
+ *    unsupported shapes) return before anything is launched.
+ *  - Data errors found on the device (a NaN score in the document span, a
+ *    kept index outside [0, N), a wait that gave up) set bits in a sticky
+ *    per-device status word read by tg_get_device_status.  Kernels never
+ *    trap; on such an error their outputs are unspecified.
+ *  - Outputs must not overlap inputs unless a call says otherwise.
+ */
+#ifndef TOKENGATE_H
+#define TOKENGATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared so that C callers need no CUDA
+ * headers. */
+typedef struct CUstream_st* tg_stream_t;
+
+typedef enum tg_status {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = 1,  /* bad pointer, size, span, alignment           */
+  TG_ERR_UNSUPPORTED = 2,  /* valid but not implemented (shape, dtype)     */
+  TG_ERR_CUDA = 3,         /* a CUDA runtime call failed                    */
+  TG_ERR_NAN_SCORE = 4,    /* device: NaN score inside the document span    */
+  TG_ERR_BAD_INDEX = 5,    /* device: a gathered index outside [0, N)       */
+  TG_ERR_TIMEOUT = 6       /* device: a pipeline wait gave up (bounded)     */
+} tg_status;
+
+typedef enum tg_dtype { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* tg_status_string(int status);
+
+/* ABI version of this header (bumped on any signature change). */
+#define TG_ABI_VERSION 1
+int tg_abi_version(void);
+
+/* Message of the last TG_ERR_INVALID_ARG / TG_ERR_UNSUPPORTED / TG_ERR_CUDA
+ * returned on the calling host thread ("" if none).  Host pointer, valid
+ * until the next call on this thread. */
+const char* tg_last_error_message(void);
+
+/*
+ * Gate MLP ([DE] "Wie hat TokenGate das Pruning von Tokens verstanden?",
+ * Gate-Modul; [TH] phase 2): one scalar score per token from its residual
+ * row at the gate layer,
+ *   s_i = sum_k w2[k] * GELU(sum_c W1[k][c] * X[i][c] + b1[k]) + b2,
+ * GELU(z) = z * Phi(z) (the exact erf form).
+ *
+ *  X       [N][d] in `dtype` (TG_BF16: tcgen05 tensor-core path, fp32
+ *          accumulation; TG_F32: CUDA-core fp32 path).
+ *  W1      [Hg][d] in `dtype` (nn.Linear layout, out x in).
+ *  b1      [Hg] fp32, or NULL for zero.
+ *  w2      [Hg] fp32.   b2: scalar.
+ *  scores  [N] fp32 output.
+ * Limits: N >= 0 (N == 0 launches nothing); d % 64 == 0 for TG_BF16
+ * (d % 4 == 0 for TG_F32); 16 <= Hg <= 256 and Hg % 16 == 0 for TG_BF16,
+ * 1 <= Hg <= 1024 for TG_F32.
+ */
+tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d,
+                        const void* W1, const float* b1, int32_t Hg,
+                        const float* w2, float b2, float* scores,
+                        tg_stream_t stream);
+
+/*
+ * Top-K select ([DE] same section: after scoring, the gate keeps the K
+ * best-scoring tokens, and only document tokens are candidates for removal,
+ * never the question; [TH] phases 2-3).
+ *
+ * Keeps every token outside [doc_begin, doc_end) and the K document tokens
+ * that come first in the order (fp32 score bit pattern as a total order
+ * descending, -0.0 below +0.0, then lower index first), and writes their
+ * indices to kept_idx in ascending order.  The result is unique, so the
+ * call is deterministic and bit-exact.
+ *
+ *  scores    [N] fp32.
+ *  kept_idx  [M] int32 output, M = N - (doc_end - doc_begin) + K.
+ *  M_out     host pointer (nullable): receives M, computed on the host, so
+ *            no device synchronisation is needed to size the next calls.
+ * Limits: 0 <= doc_begin <= doc_end <= N < 2^31, 0 <= K <= doc_end -
+ * doc_begin.  M == 0 launches nothing.  A NaN score inside the span sets
+ * TG_ERR_NAN_SCORE in the device status word (NaN then ranks above +inf).
+ * One 8-CTA cluster does the whole selection; no workspace is needed.
+ */
+tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin,
+                         int64_t doc_end, int64_t K, int32_t* kept_idx,
+                         int64_t* M_out, tg_stream_t stream);
+
+/*
+ * Row gather ([IT] "TokenGate impara quali token mantenere": only the kept
+ * tokens' representations go up; [DE] "Was ist token-gated Attention?":
+ * their scores become the attention bias):
+ *   Y[m] = X[idx[m]]                      (exact copy, or bf16 -> fp32 widen)
+ *   logsig_kept[m] = log(sigmoid(scores[idx[m]]))   (fp32, stable form)
+ *
+ *  X      [N][d] in x_dtype.     idx: [M] int32, or NULL for the identity
+ *         (then M must equal N).
+ *  Y      [M][d] in y_dtype; (x_dtype, y_dtype) is (bf16, bf16), (f32, f32)
+ *         or (bf16, f32).
+ *  scores [N] fp32 and logsig_kept [M] fp32: both NULL or both given.
+ * M == 0 launches nothing.  An index outside [0, N) sets TG_ERR_BAD_INDEX
+ * and that row is zeroed.
+ */
+tg_status tg_gather_rows(const void* X, tg_dtype x_dtype, int64_t N,
+                         int32_t d, const int32_t* idx, int64_t M, void* Y,
+                         tg_dtype y_dtype, const float* scores,
+                         float* logsig_kept, tg_stream_t stream);
+
+/*
+ * RMSNorm of a pruned layer's input (the pages' pruned layers are ordinary
+ * decoder layers run on the kept rows, [DE] "Prune-Front-Behandlung"):
+ *   Y[i][c] = X[i][c] * gamma[c] / sqrt(mean_c(X[i][c]^2) + eps)
+ *  X [M][d] in x_dtype (f32 or bf16); Y [M][d] in y_dtype (bf16 or f32).
+ *  gamma [d] fp32.  d % 8 == 0.
+ */
+tg_status tg_rmsnorm(const void* X, tg_dtype x_dtype, int64_t M, int32_t d,
+                     const float* gamma, float eps, void* Y, tg_dtype y_dtype,
+                     tg_stream_t stream);
+
+/*
+ * QKV projection of the kept rows (layers above L, [DE] "Prune-Front-
+ * Behandlung": no KV is produced for pruned tokens):
+ *   QKV = X * Wqkv^T,  Wqkv [(Hq + 2 Hkv) * dh][d] (nn.Linear layout):
+ *   output columns [0, Hq dh) are q heads, then Hkv dh of k, then Hkv dh
+ *   of v.  TG_BF16: tcgen05 GEMM, fp32 accumulation, bf16 output rounded
+ *   to nearest-even.  TG_F32: fp32 CUDA-core GEMM.
+ *  X [M][d], QKV [M][(Hq + 2 Hkv) dh], both in `dtype`.
+ * Limits: d % 64 == 0 and (Hq + 2 Hkv) dh % 16 == 0 for TG_BF16;
+ * d % 4 == 0 for TG_F32.
+ */
+tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d,
+                      const void* Wqkv, int32_t Hq, int32_t Hkv, int32_t dh,
+                      void* QKV, tg_stream_t stream);
+
+/*
+ * Token-gated causal attention over the kept rows ([DE] "Was ist
+ * token-gated Attention?"; [TH] token-gated attention, per-head gain and
+ * learnable temperature; [RU] "Механизм token-gated attention"):
+ *   l_ij = t * (q_i . k_j) / sqrt(dh) + g_h * logsig_kept[j],  j <= i
+ *   o_i  = sum_j softmax_j(l_ij) v_j,   kv head of q head h = h / (Hq/Hkv)
+ * Rows are the kept tokens in ascending original order, so causality on
+ * row numbers equals causality on original positions.
+ *
+ *  QKV          [M][(Hq + 2 Hkv) dh] in `dtype` (layout of tg_qkv_proj).
+ *  logsig_kept  [M] fp32, or NULL for no bias (plain causal attention, the
+ *               full-prefill path).
+ *  gain         [Hq] fp32 (ignored when logsig_kept is NULL).
+ *  temperature  scalar t.
+ *  O            [M][Hq dh] in `dtype`, or NULL when residual is given.
+ *  residual     [M][Hq dh] fp32 or NULL: when given, residual += o in fp32
+ *               (the layer's residual add), fused into the epilogue.
+ * Limits: Hq % Hkv == 0.  TG_BF16: dh == 128 and (Hq / Hkv) even.
+ * TG_F32: dh <= 128 and dh % 4 == 0.
+ */
+tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M,
+                          int32_t Hq, int32_t Hkv, int32_t dh,
+                          const float* logsig_kept, const float* gain,
+                          float temperature, void* O, float* residual,
+                          tg_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the sticky device status
+ * of the current device: TG_OK, or the first of TG_ERR_NAN_SCORE,
+ * TG_ERR_BAD_INDEX, TG_ERR_TIMEOUT that is set.  TG_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+tg_status tg_get_device_status(tg_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* TOKENGATE_H */

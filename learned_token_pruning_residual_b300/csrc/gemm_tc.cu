@@ -1,0 +1,287 @@
+// tcgen05 GEMMs of the gated prefill, bf16 in / fp32 accumulate:
+//
+//  * gate scoring (TokenGate pages, spke.com "TokenGate – Token-Gated
+//    Attention macht das Vollfüllen von langen Kontexten bis zu 11,3-mal
+//    schneller", section "Wie hat TokenGate das Pruning von Tokens
+//    verstanden?", Gate-Modul): Z = X W1^T with the MLP head fused into the
+//    epilogue, s = w2 . GELU(Z + b1) + b2, so Z never leaves the SM;
+//  * the QKV projection of the kept rows (the pruned layers above the gate,
+//    same section): QKV = X Wqkv^T, stored as bf16.
+//
+// One persistent CTA per SM walks output tiles of 128 x BN.  Warp 0 streams
+// 128 x 64 A and BN x 64 B tiles into a STAGES-deep ring with TMA (128-byte
+// swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=BN, K=16)
+// into one of two TMEM accumulators; warps 2-5 drain the other accumulator
+// (one row per thread via tcgen05.ld) while the next tile accumulates.
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+enum { EPI_STORE_BF16 = 0, EPI_GATE = 1 };
+
+struct GemmArgs {
+  int M, N, K;
+  int tiles_n, num_tiles;
+  __nv_bfloat16* C;  // EPI_STORE_BF16: [M][ldc]
+  int64_t ldc;
+  const float* b1;  // EPI_GATE: N = Hg <= BN
+  const float* w2;
+  float b2;
+  float* scores;
+  uint32_t* status;
+};
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  uint8_t a[STAGES][BM * BK * 2];  // each 16 KB, 1024-aligned
+  uint8_t b[STAGES][BN * BK * 2];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float b1[256];
+  float w2[256];
+};
+
+__device__ __forceinline__ float gelu_erf(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  using Smem = GemmSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr uint32_t kStageBytes = (BM + BN) * BK * 2;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, 0, 0);
+  volatile int* abort = &S.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&S.full[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&S.acc_full[b]), 1);
+      mbar_init(smem_u32(&S.acc_empty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&S.drain), 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (EPI == EPI_GATE && warp >= 2) {
+    for (int i = threadIdx.x - 64; i < BN; i += 32 * kEpiWarps) {
+      S.b1[i] = (i < args.N && args.b1 != nullptr) ? args.b1[i] : 0.f;
+      S.w2[i] = (i < args.N) ? args.w2[i] : 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const int k_blocks = (args.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- TMA producer
+      const uint64_t pol_a = EPI == EPI_GATE ? l2_policy_evict_first() : l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+        const int tm = tile / args.tiles_n, tn = tile - tm * args.tiles_n;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&S.full[s]);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d_hint(smem_u32(S.a[s]), &tmA, fb, kb * BK, tm * BM, pol_a);
+          tma_load_2d_hint(smem_u32(S.b[s]), &tmB, fb, kb * BK, tn * BN, pol_b);
+          ++it;
+        }
+      }
+      // every issued fill lands before the CTA may exit
+      for (uint32_t s = 0; s < STAGES && s < it; ++s) {
+        const uint32_t last = ((it - 1 - s) / STAGES) * STAGES + s;
+        mbar_wait_drain(smem_u32(&S.full[s]), (last / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------ MMA issuer
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++local) {
+        const uint32_t buf = local & 1, aph = (local >> 1) & 1;
+        if (!mbar_wait(smem_u32(&S.acc_empty[buf]), aph ^ 1, abort, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          if (!mbar_wait(smem_u32(&S.full[s]), ph, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_ss(d_tmem, smem_desc_sw128(a0 + k * 32, 16, 1024),
+                   smem_desc_sw128(b0 + k * 32, 16, 1024), kIdesc, (kb | k) != 0);
+          }
+          mma_commit(smem_u32(&S.empty[s]));
+        }
+        if (ok) mma_commit(smem_u32(&S.acc_full[buf]));
+      }
+      // all MMAs of this thread complete before TMEM is released
+      mma_commit(smem_u32(&S.drain));
+      mbar_wait_drain(smem_u32(&S.drain), 0);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // the TMEM lane quadrant this warp may read
+    const int r_in_tile = q * 32 + lane;
+    uint32_t local = 0;
+    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
+      const uint32_t buf = local & 1, aph = (local >> 1) & 1;
+      if (!mbar_wait(smem_u32(&S.acc_full[buf]), aph, abort, args.status)) break;
+      tc_fence_after();
+      const int tm = tile / args.tiles_n, tn = tile - tm * args.tiles_n;
+      const int64_t row = static_cast<int64_t>(tm) * BM + r_in_tile;
+      const bool row_ok = row < args.M;
+      const uint32_t t_row = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+      if constexpr (EPI == EPI_STORE_BF16) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_row + c0, r);
+          tmem_ld_wait();
+          const int col0 = tn * BN + c0;
+          if (row_ok && col0 < args.N) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            __nv_bfloat16* dst = args.C + row * args.ldc + col0;
+            if (col0 + 32 <= args.N) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            } else {
+              uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+              for (int i = 0; i < 32 && col0 + i < args.N; ++i)
+                d16[i] = static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
+            }
+          }
+        }
+      } else {
+        float acc = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (c0 >= args.N) break;
+          uint32_t r[32];
+          tmem_ld32(t_row + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float z = __uint_as_float(r[i]) + S.b1[c0 + i];
+            acc = fmaf(S.w2[c0 + i], gelu_erf(z), acc);  // padded columns have w2 = 0
+          }
+        }
+        if (row_ok) args.scores[row] = acc + args.b2;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.acc_empty[buf]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, int EPI>
+cudaError_t launch_gemm(const void* A, const void* B, const GemmArgs& a0, cudaStream_t stream) {
+  GemmArgs args = a0;
+  args.tiles_n = (args.N + BN - 1) / BN;
+  const int tiles_m = (args.M + BM - 1) / BM;
+  args.num_tiles = tiles_m * args.tiles_n;
+  args.status = device_status_word();
+  if (args.num_tiles == 0) return cudaSuccess;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, args.M,
+                    static_cast<uint64_t>(args.K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, args.N,
+                    static_cast<uint64_t>(args.K) * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  auto kernel = gemm_bf16_tc_kernel<BN, STAGES, EPI>;
+  const size_t smem = sizeof(GemmSmem<BN, STAGES>) + 1024;
+  cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int grid = args.num_tiles < sm_count() ? args.num_tiles : sm_count();
+  kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gate_bf16(const void* X, int64_t N, int d, const void* W1, const float* b1,
+                             int Hg, const float* w2, float b2, float* scores,
+                             cudaStream_t stream) {
+  GemmArgs a{};
+  a.M = static_cast<int>(N);
+  a.N = Hg;
+  a.K = d;
+  a.b1 = b1;
+  a.w2 = w2;
+  a.b2 = b2;
+  a.scores = scores;
+  if (Hg <= 128) return launch_gemm<128, 6, EPI_GATE>(X, W1, a, stream);
+  return launch_gemm<256, 4, EPI_GATE>(X, W1, a, stream);
+}
+
+cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int ncols, void* Y,
+                            cudaStream_t stream) {
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = ncols;
+  a.K = d;
+  a.C = static_cast<__nv_bfloat16*>(Y);
+  a.ldc = ncols;
+  return launch_gemm<256, 4, EPI_STORE_BF16>(X, W, a, stream);
+}
+
+}  // namespace tg

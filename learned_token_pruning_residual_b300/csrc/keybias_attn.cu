@@ -1,0 +1,411 @@
+// Token-gated causal attention over the kept rows, bf16 in / fp32 softmax,
+// on tcgen05 tensor cores (TokenGate pages: spke.com "TokenGate – Token-
+// Gated Attention macht das Vollfüllen von langen Kontexten bis zu 11,3-mal
+// schneller", section "Was ist token-gated Attention?": each kept token's
+// gate score becomes a bias on the attention logits, with a learnable gain
+// per head and a learnable temperature; ai4bro.com, section "กลไกการทำงาน
+// ของ Learned Token Pruning"):
+//
+//   l_ij = t (q_i . k_j) / sqrt(128) + g_h ls_j   (j <= i),   o_i = softmax_j(l_ij) v_j
+//
+// Layout of one CTA (one 128-row query block, two q heads h0, h0+1 of one
+// kv head, so every K/V tile is loaded once and used by both heads):
+//   warp 0      TMA: Q tiles of both heads once, then K_j, V_j (128 x 128
+//               bf16, 128-byte swizzle, 2-deep rings) and the bias inputs
+//               ls_j (128 fp32) per key tile j = 0 .. (causal) block index.
+//   warp 1      one thread issues tcgen05.mma: S_t = Q_t K_j^T into TMEM
+//               (SS form), and O_t += P_t V_j with P_t read from TMEM (TS
+//               form, V MN-major).
+//   warps 4-7   softmax + epilogue of head h0 (t = 0), one query row per
+//   warps 8-11  thread, likewise for head h1 (t = 1).
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each; P_t (bf16
+// pairs) overwrites the first 64 columns of S_t once S_t is in registers.
+// The two heads ping-pong: while softmax t works, the tensor cores run
+// head 1-t.  The running max is only raised when a row's max grows by more
+// than 2^8 (log2 units), so O is rescaled in TMEM rarely; the final division
+// by the row sum makes the result exact either way.  Causal tile skipping:
+// query block b only visits key tiles 0..b; only tile b is masked.
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+constexpr int kBQ = 128;  // query rows per block
+constexpr int kBK = 128;  // keys per tile
+constexpr int kDH = 128;  // head dim
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = kBK * kDH * 2;  // 32 KB
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct AttnArgs {
+  int M, Hq, Hkv, G;
+  int n_rb, pairs_per_kv;
+  float scale2;  // t / sqrt(dh) * log2(e)
+  const float* gain;
+  __nv_bfloat16* O;
+  float* residual;
+  int64_t ldo;  // Hq * dh
+  uint32_t* status;
+};
+
+struct AttnSmem {
+  uint8_t q[2][kTileBytes];
+  uint8_t k[2][kTileBytes];
+  uint8_t v[2][kTileBytes];
+  float ls[2][kBK];
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t ls_full[2], ls_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// One lane waits, the warp follows: keeps the .sync.aligned tcgen05 ops
+// below warp-uniform even when a wait gives up.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+template <bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1)
+    keybias_attn_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                        const __grid_constant__ CUtensorMap tm_ls, const AttnArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  AttnSmem& S = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &S.abort;
+
+  // work unit: heaviest query blocks first
+  const int units_per_rb = args.Hkv * args.pairs_per_kv;
+  const int rb = args.n_rb - 1 - static_cast<int>(blockIdx.x) / units_per_rb;
+  const int rem = static_cast<int>(blockIdx.x) % units_per_rb;
+  const int hk = rem / args.pairs_per_kv;
+  const int h0 = hk * args.G + 2 * (rem % args.pairs_per_kv);
+  const int nkv = rb + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&S.q_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&S.k_full[s]), 1);
+      mbar_init(smem_u32(&S.k_empty[s]), 1);
+      mbar_init(smem_u32(&S.v_full[s]), 1);
+      mbar_init(smem_u32(&S.v_empty[s]), 1);
+      mbar_init(smem_u32(&S.ls_full[s]), 1);
+      mbar_init(smem_u32(&S.ls_empty[s]), 8);  // 4 warps x 2 heads
+      mbar_init(smem_u32(&S.s_full[s]), 1);
+      mbar_init(smem_u32(&S.p_full[s]), 4);
+      mbar_init(smem_u32(&S.o_done[s]), 1);
+    }
+    mbar_init(smem_u32(&S.drain), 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_qkv);
+    if (BIAS) tma_prefetch_desc(&tm_ls);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&S.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- TMA
+      const int kcol = (args.Hq + hk) * kDH;
+      const int vcol = (args.Hq + args.Hkv + hk) * kDH;
+      const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by later blocks
+      mbar_arrive_expect_tx(smem_u32(&S.q_full), 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_2d(smem_u32(S.q[t]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full),
+                      (h0 + t) * kDH + bx * 64, rb * kBQ);
+      int nk = 0, nls = 0, nv = 0;  // fills issued per ring
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status)) break;
+        mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_2d_hint(smem_u32(S.k[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.k_full[s]),
+                           kcol + bx * 64, j * kBK, pol);
+        ++nk;
+        if (BIAS) {
+          if (!mbar_wait(smem_u32(&S.ls_empty[s]), ph ^ 1, abort, args.status)) break;
+          mbar_arrive_expect_tx(smem_u32(&S.ls_full[s]), kBK * 4);
+          tma_load_1d(smem_u32(S.ls[s]), &tm_ls, smem_u32(&S.ls_full[s]), j * kBK);
+          ++nls;
+        }
+        if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort, args.status)) break;
+        mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_2d_hint(smem_u32(S.v[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.v_full[s]),
+                           vcol + bx * 64, j * kBK, pol);
+        ++nv;
+      }
+      // drain: every issued copy lands before the CTA may exit.  A fill that
+      // was already consumed has completed its phase, so in the normal case
+      // these waits return at once.
+      mbar_wait_drain(smem_u32(&S.q_full), 0);
+      for (int s = 0; s < 2; ++s) {
+        if (s < nk) mbar_wait_drain(smem_u32(&S.k_full[s]), (((nk - 1 - s) >> 1) & 1));
+        if (s < nls) mbar_wait_drain(smem_u32(&S.ls_full[s]), (((nls - 1 - s) >> 1) & 1));
+        if (s < nv) mbar_wait_drain(smem_u32(&S.v_full[s]), (((nv - 1 - s) >> 1) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
+      bool ok = mbar_wait(smem_u32(&S.q_full), 0, abort, args.status);
+      tc_fence_after();
+      for (int j = 0; ok && j <= nkv; ++j) {
+        const int s = j & 1;
+        if (j < nkv) {
+          ok = mbar_wait(smem_u32(&S.k_full[s]), (j >> 1) & 1, abort, args.status);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        for (int t = 0; ok && t < 2; ++t) {
+          if (j > 0) {
+            const int jp = j - 1, sp = jp & 1;
+            if (t == 0) {
+              ok = mbar_wait(smem_u32(&S.v_full[sp]), (jp >> 1) & 1, abort, args.status);
+              if (!ok) break;
+            }
+            ok = mbar_wait(smem_u32(&S.p_full[t]), jp & 1, abort, args.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t o_tmem = tmem + 256 + t * 128;
+            const uint32_t p_tmem = tmem + t * 128;
+            const uint32_t v0 = smem_u32(S.v[sp]);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(v0 + kk * 2048, kHalfBytes, 1024),
+                     idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&S.o_done[t]));
+            if (t == 1) mma_commit(smem_u32(&S.v_empty[sp]));
+          }
+          if (j < nkv) {
+            const uint32_t q0 = smem_u32(S.q[t]), k0 = smem_u32(S.k[s]);
+            const uint32_t s_tmem = tmem + t * 128;
+#pragma unroll
+            for (int kk = 0; kk < kDH / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+              mma_ss(s_tmem, smem_desc_sw128(q0 + off, 16, 1024),
+                     smem_desc_sw128(k0 + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&S.s_full[t]));
+          }
+        }
+        if (ok && j < nkv) mma_commit(smem_u32(&S.k_empty[s]));
+      }
+      mma_commit(smem_u32(&S.drain));
+      mbar_wait_drain(smem_u32(&S.drain), 0);
+    }
+  } else if (warp >= 4) {
+    // --------------------------------------------------- softmax + epilogue
+    const int t = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // row within the block
+    const int64_t row = static_cast<int64_t>(rb) * kBQ + r;
+    const int h = h0 + t;
+    const float scale2 = args.scale2;
+    const float g2 = BIAS ? args.gain[h] * kLog2e : 0.f;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_tmem = tmem + t * 128 + lane_off;
+    const uint32_t o_tmem = tmem + 256 + t * 128 + lane_off;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int s = j & 1;
+      if (!(ok = warp_wait(smem_u32(&S.s_full[t]), j & 1, abort, args.status))) break;
+      if (BIAS && !(ok = warp_wait(smem_u32(&S.ls_full[s]), (j >> 1) & 1, abort, args.status)))
+        break;
+      tc_fence_after();
+      float x[kBK];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int c0 = 0; c0 < kBK; c0 += 32) {
+          tmem_ld32(s_tmem + c0, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(u[i]);
+        }
+      }
+      if (BIAS) {
+        const float4* lv = reinterpret_cast<const float4*>(S.ls[s]);
+#pragma unroll
+        for (int c4 = 0; c4 < kBK / 4; ++c4) {
+          const float4 b = lv[c4];
+          x[4 * c4 + 0] = fmaf(x[4 * c4 + 0], scale2, g2 * b.x);
+          x[4 * c4 + 1] = fmaf(x[4 * c4 + 1], scale2, g2 * b.y);
+          x[4 * c4 + 2] = fmaf(x[4 * c4 + 2], scale2, g2 * b.z);
+          x[4 * c4 + 3] = fmaf(x[4 * c4 + 3], scale2, g2 * b.w);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.ls_empty[s]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBK; ++c) x[c] *= scale2;
+      }
+      if (j == rb) {  // the diagonal tile: key c is row rb*128 + c
+#pragma unroll
+        for (int c = 0; c < kBK; ++c)
+          if (c > r) x[c] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < kBK; ++c) mx = fmaxf(mx, x[c]);
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = m_new > m_run + kRescaleThreshold;
+      const float m_old = m_run;
+      if (need) m_run = m_new;
+      // p = 2^(x - m_run), packed to bf16 pairs into the first 64 columns of S_t
+      float sum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = exp2_approx(x[64 * half + 2 * i] - m_run);
+          const float p1 = exp2_approx(x[64 * half + 2 * i + 1] - m_run);
+          sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_tmem + 32 * half, pk);
+      }
+      tmem_st_wait();
+      // raise O to the new max once the previous P V is done with it
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+        if (!(ok = warp_wait(smem_u32(&S.o_done[t]), (j - 1) & 1, abort, args.status))) break;
+        tc_fence_after();
+        const float f = need ? exp2_approx(m_old - m_new) : 1.f;
+        l_run *= f;
+        uint32_t u[32];
+#pragma unroll
+        for (int c0 = 0; c0 < kDH; c0 += 32) {
+          tmem_ld32(o_tmem + c0, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+          tmem_st32(o_tmem + c0, u);
+        }
+        tmem_st_wait();
+      }
+      l_run += sum;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.p_full[t]));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && warp_wait(smem_u32(&S.o_done[t]), (nkv - 1) & 1, abort, args.status)) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      const bool row_ok = row < args.M;
+      uint32_t u[32];
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDH; c0 += 32) {
+        tmem_ld32(o_tmem + c0, u);
+        tmem_ld_wait();
+        if (row_ok) {
+          if (args.residual != nullptr) {
+            float4* dst = reinterpret_cast<float4*>(args.residual + row * args.ldo + h * kDH + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 a = dst[i];
+              a.x += __uint_as_float(u[4 * i + 0]) * inv;
+              a.y += __uint_as_float(u[4 * i + 1]) * inv;
+              a.z += __uint_as_float(u[4 * i + 2]) * inv;
+              a.w += __uint_as_float(u[4 * i + 3]) * inv;
+              dst[i] = a;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(args.O + row * args.ldo + h * kDH + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv, __uint_as_float(u[8 * i + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv);
+              dst[i] = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
+                             const float* logsig, const float* gain, float temperature, void* O,
+                             float* residual, cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  AttnArgs a{};
+  a.M = static_cast<int>(M);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.n_rb = static_cast<int>((M + kBQ - 1) / kBQ);
+  a.pairs_per_kv = a.G / 2;
+  a.scale2 = temperature / sqrtf(static_cast<float>(dh)) * kLog2e;
+  a.gain = gain;
+  a.O = static_cast<__nv_bfloat16*>(O);
+  a.residual = residual;
+  a.ldo = static_cast<int64_t>(Hq) * dh;
+  a.status = device_status_word();
+  const int cols = (Hq + 2 * Hkv) * dh;
+  CUtensorMap tm_qkv, tm_ls;
+  if (!make_tmap_2d(&tm_qkv, QKV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, M,
+                    static_cast<uint64_t>(cols) * 2, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (logsig != nullptr) {
+    if (!make_tmap_1d_f32(&tm_ls, logsig, M, kBK)) return cudaErrorInvalidValue;
+  } else {
+    tm_ls = tm_qkv;  // unused
+  }
+  const size_t smem = sizeof(AttnSmem) + 1024;
+  const int grid = a.n_rb * Hkv * a.pairs_per_kv;
+  if (logsig != nullptr) {
+    cudaError_t err = cudaFuncSetAttribute(keybias_attn_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    keybias_attn_kernel<true><<<grid, kThreads, smem, stream>>>(tm_qkv, tm_ls, a);
+  } else {
+    cudaError_t err = cudaFuncSetAttribute(keybias_attn_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    keybias_attn_kernel<false><<<grid, kThreads, smem, stream>>>(tm_qkv, tm_ls, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tg

@@ -1,0 +1,303 @@
+// The C ABI of libtokengate.so: argument checks, the sticky device status
+// word, tensor-map encoding, and dispatch to the kernels.  Every check that
+// can fail happens here, before anything is launched.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "tg_device.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+
+// The sticky per-device status word.  Kernels OR error bits into it;
+// tg_get_device_status reads and clears it.
+__device__ uint32_t g_status_word = 0;
+
+namespace {
+thread_local char t_last_error[512] = "";
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool load_encode() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+}  // namespace
+
+tg_status fail(tg_status code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+uint32_t* device_status_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                  uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+                  uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  (void)elem_bytes;
+  if (!load_encode()) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_1d_f32(CUtensorMap* map, const float* base, uint64_t n, uint32_t box) {
+  if (!load_encode()) return false;
+  const cuuint64_t dims[1] = {n};
+  const cuuint64_t strides[1] = {n * 4};
+  const cuuint32_t boxd[1] = {box};
+  const cuuint32_t estr[1] = {1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(base), dims,
+                  strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tg
+
+using tg::fail;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tg_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return TG_OK;
+  return fail(TG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define TG_REQUIRE(cond, code, ...) \
+  do {                              \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* tg_status_string(int status) {
+  switch (status) {
+    case TG_OK: return "TG_OK";
+    case TG_ERR_INVALID_ARG: return "TG_ERR_INVALID_ARG";
+    case TG_ERR_UNSUPPORTED: return "TG_ERR_UNSUPPORTED";
+    case TG_ERR_CUDA: return "TG_ERR_CUDA";
+    case TG_ERR_NAN_SCORE: return "TG_ERR_NAN_SCORE";
+    case TG_ERR_BAD_INDEX: return "TG_ERR_BAD_INDEX";
+    case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT";
+    default: return "TG_ERR_UNKNOWN";
+  }
+}
+
+int tg_abi_version(void) { return TG_ABI_VERSION; }
+
+const char* tg_last_error_message(void) { return tg::t_last_error; }
+
+tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d, const void* W1,
+                        const float* b1, int32_t Hg, const float* w2, float b2, float* scores,
+                        tg_stream_t stream) {
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "gate: bad dtype");
+  TG_REQUIRE(N >= 0 && N < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "gate: N out of range");
+  TG_REQUIRE(d > 0 && Hg > 0, TG_ERR_INVALID_ARG, "gate: d and Hg must be positive");
+  if (N == 0) return TG_OK;
+  TG_REQUIRE(X && W1 && w2 && scores, TG_ERR_INVALID_ARG, "gate: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(W1) && aligned16(w2) && aligned16(scores) &&
+                 (!b1 || aligned16(b1)),
+             TG_ERR_INVALID_ARG, "gate: pointers must be 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TG_BF16) {
+    TG_REQUIRE(d % 64 == 0, TG_ERR_UNSUPPORTED, "gate bf16: d %% 64 != 0 (d=%d)", d);
+    TG_REQUIRE(Hg >= 16 && Hg <= 256 && Hg % 16 == 0, TG_ERR_UNSUPPORTED,
+               "gate bf16: need 16 <= Hg <= 256, Hg %% 16 == 0 (Hg=%d)", Hg);
+    return from_cuda(tg::launch_gate_bf16(X, N, d, W1, b1, Hg, w2, b2, scores, st), "gate bf16");
+  }
+  TG_REQUIRE(d % 4 == 0, TG_ERR_UNSUPPORTED, "gate f32: d %% 4 != 0");
+  TG_REQUIRE(Hg <= 1024, TG_ERR_UNSUPPORTED, "gate f32: Hg > 1024");
+  TG_REQUIRE(static_cast<int64_t>(d) * 4 <= 200 * 1024, TG_ERR_UNSUPPORTED, "gate f32: d too big");
+  return from_cuda(tg::launch_gate_f32(static_cast<const float*>(X), N, d,
+                                       static_cast<const float*>(W1), b1, Hg, w2, b2, scores, st),
+                   "gate f32");
+}
+
+tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin, int64_t doc_end,
+                         int64_t K, int32_t* kept_idx, int64_t* M_out, tg_stream_t stream) {
+  TG_REQUIRE(N >= 0 && N < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "select: N out of range");
+  TG_REQUIRE(0 <= doc_begin && doc_begin <= doc_end && doc_end <= N, TG_ERR_INVALID_ARG,
+             "select: need 0 <= doc_begin <= doc_end <= N");
+  TG_REQUIRE(0 <= K && K <= doc_end - doc_begin, TG_ERR_INVALID_ARG,
+             "select: need 0 <= K <= doc_end - doc_begin");
+  const int64_t M = N - (doc_end - doc_begin) + K;
+  if (M_out) *M_out = M;
+  if (M == 0) return TG_OK;  // nothing to write: nothing is launched
+  TG_REQUIRE(scores && kept_idx, TG_ERR_INVALID_ARG, "select: NULL pointer");
+  TG_REQUIRE(aligned16(scores) && aligned16(kept_idx), TG_ERR_INVALID_ARG,
+             "select: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_select(scores, N, doc_begin, doc_end, K, kept_idx,
+                                     reinterpret_cast<cudaStream_t>(stream)),
+                   "select");
+}
+
+tg_status tg_gather_rows(const void* X, tg_dtype x_dtype, int64_t N, int32_t d,
+                         const int32_t* idx, int64_t M, void* Y, tg_dtype y_dtype,
+                         const float* scores, float* logsig_kept, tg_stream_t stream) {
+  TG_REQUIRE((x_dtype == TG_BF16 && (y_dtype == TG_BF16 || y_dtype == TG_F32)) ||
+                 (x_dtype == TG_F32 && y_dtype == TG_F32),
+             TG_ERR_UNSUPPORTED, "gather: dtype pair not supported");
+  TG_REQUIRE(N >= 0 && M >= 0 && d > 0, TG_ERR_INVALID_ARG, "gather: bad sizes");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(idx != nullptr || M == N, TG_ERR_INVALID_ARG, "gather: idx NULL needs M == N");
+  TG_REQUIRE((scores == nullptr) == (logsig_kept == nullptr), TG_ERR_INVALID_ARG,
+             "gather: scores and logsig_kept must both be given or both NULL");
+  const int64_t in_row = static_cast<int64_t>(d) * (x_dtype == TG_BF16 ? 2 : 4);
+  TG_REQUIRE(in_row % 16 == 0, TG_ERR_INVALID_ARG, "gather: row bytes must be a multiple of 16");
+  TG_REQUIRE(X && Y, TG_ERR_INVALID_ARG, "gather: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(Y) && (!idx || aligned16(idx)) &&
+                 (!scores || aligned16(scores)) && (!logsig_kept || aligned16(logsig_kept)),
+             TG_ERR_INVALID_ARG, "gather: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_gather(X, x_dtype == TG_BF16, N, d, idx, M, Y, y_dtype == TG_BF16,
+                                     scores, logsig_kept, reinterpret_cast<cudaStream_t>(stream)),
+                   "gather");
+}
+
+tg_status tg_rmsnorm(const void* X, tg_dtype x_dtype, int64_t M, int32_t d, const float* gamma,
+                     float eps, void* Y, tg_dtype y_dtype, tg_stream_t stream) {
+  TG_REQUIRE((x_dtype == TG_F32 || x_dtype == TG_BF16) && (y_dtype == TG_F32 || y_dtype == TG_BF16),
+             TG_ERR_INVALID_ARG, "rmsnorm: bad dtype");
+  TG_REQUIRE(M >= 0 && d > 0 && d % 8 == 0, TG_ERR_INVALID_ARG, "rmsnorm: need d %% 8 == 0");
+  TG_REQUIRE(eps >= 0.f, TG_ERR_INVALID_ARG, "rmsnorm: eps < 0");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(X && Y && gamma, TG_ERR_INVALID_ARG, "rmsnorm: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(Y) && aligned16(gamma), TG_ERR_INVALID_ARG,
+             "rmsnorm: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_rmsnorm(X, x_dtype == TG_BF16, M, d, gamma, eps, Y,
+                                      y_dtype == TG_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                   "rmsnorm");
+}
+
+tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d, const void* Wqkv,
+                      int32_t Hq, int32_t Hkv, int32_t dh, void* QKV, tg_stream_t stream) {
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "qkv: bad dtype");
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && d > 0 && Hq > 0 && Hkv > 0 && dh > 0,
+             TG_ERR_INVALID_ARG, "qkv: bad sizes");
+  const int64_t cols = static_cast<int64_t>(Hq + 2 * Hkv) * dh;
+  TG_REQUIRE(cols < (int64_t(1) << 20), TG_ERR_INVALID_ARG, "qkv: too many columns");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(X && Wqkv && QKV, TG_ERR_INVALID_ARG, "qkv: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(Wqkv) && aligned16(QKV), TG_ERR_INVALID_ARG,
+             "qkv: pointers must be 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TG_BF16) {
+    TG_REQUIRE(d % 64 == 0, TG_ERR_UNSUPPORTED, "qkv bf16: d %% 64 != 0");
+    TG_REQUIRE(cols % 16 == 0, TG_ERR_UNSUPPORTED, "qkv bf16: output columns %% 16 != 0");
+    return from_cuda(tg::launch_qkv_bf16(X, M, d, Wqkv, static_cast<int>(cols), QKV, st),
+                     "qkv bf16");
+  }
+  TG_REQUIRE(d % 4 == 0, TG_ERR_UNSUPPORTED, "qkv f32: d %% 4 != 0");
+  return from_cuda(tg::launch_qkv_f32(static_cast<const float*>(X), M, d,
+                                      static_cast<const float*>(Wqkv), static_cast<int>(cols),
+                                      static_cast<float*>(QKV), st),
+                   "qkv f32");
+}
+
+tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq, int32_t Hkv,
+                          int32_t dh, const float* logsig_kept, const float* gain,
+                          float temperature, void* O, float* residual, tg_stream_t stream) {
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "attn: bad dtype");
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && Hkv > 0 && dh > 0,
+             TG_ERR_INVALID_ARG, "attn: bad sizes");
+  TG_REQUIRE(Hq % Hkv == 0, TG_ERR_INVALID_ARG, "attn: Hq %% Hkv != 0");
+  TG_REQUIRE(temperature == temperature, TG_ERR_INVALID_ARG, "attn: temperature is NaN");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(QKV && (O || residual), TG_ERR_INVALID_ARG, "attn: NULL pointer");
+  TG_REQUIRE(!logsig_kept || gain, TG_ERR_INVALID_ARG, "attn: gain needed with a bias");
+  TG_REQUIRE(aligned16(QKV) && (!O || aligned16(O)) && (!residual || aligned16(residual)) &&
+                 (!logsig_kept || aligned16(logsig_kept)),
+             TG_ERR_INVALID_ARG, "attn: pointers must be 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TG_BF16) {
+    TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "attn bf16: dh must be 128");
+    TG_REQUIRE((Hq / Hkv) % 2 == 0, TG_ERR_UNSUPPORTED, "attn bf16: Hq / Hkv must be even");
+    return from_cuda(tg::launch_attn_bf16(QKV, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
+                                          residual, st),
+                     "attn bf16");
+  }
+  TG_REQUIRE(dh == 32 || dh == 64 || dh == 128, TG_ERR_UNSUPPORTED,
+             "attn f32: dh must be 32, 64 or 128");
+  return from_cuda(tg::launch_attn_f32(static_cast<const float*>(QKV), M, Hq, Hkv, dh,
+                                       logsig_kept, gain, temperature, static_cast<float*>(O),
+                                       residual, st),
+                   "attn f32");
+}
+
+tg_status tg_get_device_status(tg_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
+  uint32_t* p = tg::device_status_word();
+  if (!p) return fail(TG_ERR_CUDA, "status: no device status word");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
+  if (v != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
+  }
+  if (v & tg::kStatusNanScore) return TG_ERR_NAN_SCORE;
+  if (v & tg::kStatusBadIndex) return TG_ERR_BAD_INDEX;
+  if (v & tg::kStatusTimeout) return TG_ERR_TIMEOUT;
+  return TG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Host-side declarations shared by the library's translation units: kernel
+// launchers, tensor-map helpers and error reporting.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tokengate.h"
+
+namespace tg {
+
+// Records a message for tg_last_error_message() and returns `code`.
+tg_status fail(tg_status code, const char* fmt, ...);
+
+// Device address of the sticky status word on the current device.
+uint32_t* device_status_word();
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// 2-D tiled tensor map over a row-major matrix [rows][cols] of `elem_bytes`
+// elements whose rows are `row_bytes` apart; box = box_cols x box_rows.
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                  uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+                  uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// 1-D tiled tensor map over a vector of `n` fp32 values, box of `box` values.
+bool make_tmap_1d_f32(CUtensorMap* map, const float* base, uint64_t n, uint32_t box);
+
+// ---- launchers (argument checking happens in the ABI layer)
+cudaError_t launch_gate_bf16(const void* X, int64_t N, int d, const void* W1, const float* b1,
+                             int Hg, const float* w2, float b2, float* scores,
+                             cudaStream_t stream);
+cudaError_t launch_gate_f32(const float* X, int64_t N, int d, const float* W1, const float* b1,
+                            int Hg, const float* w2, float b2, float* scores,
+                            cudaStream_t stream);
+cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int ncols, void* Y,
+                            cudaStream_t stream);
+cudaError_t launch_qkv_f32(const float* X, int64_t M, int d, const float* W, int ncols, float* Y,
+                           cudaStream_t stream);
+cudaError_t launch_select(const float* scores, int64_t N, int64_t b, int64_t e, int64_t K,
+                          int32_t* idx, cudaStream_t stream);
+cudaError_t launch_gather(const void* X, int x_bf16, int64_t N, int d, const int32_t* idx,
+                          int64_t M, void* Y, int y_bf16, const float* scores, float* logsig,
+                          cudaStream_t stream);
+cudaError_t launch_rmsnorm(const void* X, int x_bf16, int64_t M, int d, const float* gamma,
+                           float eps, void* Y, int y_bf16, cudaStream_t stream);
+cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
+                             const float* logsig, const float* gain, float temperature, void* O,
+                             float* residual, cudaStream_t stream);
+cudaError_t launch_attn_f32(const float* QKV, int64_t M, int Hq, int Hkv, int dh,
+                            const float* logsig, const float* gain, float temperature, float* O,
+                            float* residual, cudaStream_t stream);
+
+}  // namespace tg

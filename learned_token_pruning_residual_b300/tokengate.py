@@ -1,0 +1,216 @@
+"""Thin Python binding of libtokengate.so (ctypes).
+
+Argument marshalling only: every step of the gated prefill runs in the
+library's CUDA kernels.  torch supplies device memory and the stream (the
+caller's current CUDA stream).  If the library has not been built, or no
+CUDA device is present, the calls raise; there is no fallback path.
+
+Functions carry the C names:
+
+    tg_gate_score     scores = w2 . GELU(W1 x + b1) + b2 per token
+    tg_select_topk    kept indices: non-document tokens + top-K document tokens
+    tg_gather_rows    kept rows and log(sigmoid(score)) of each kept token
+    tg_rmsnorm        RMSNorm of a pruned layer's input
+    tg_qkv_proj       packed q|k|v projection of the kept rows
+    tg_keybias_attn   causal GQA attention with the per-key bias g_h * logsig
+    tg_get_device_status
+
+plus two compositions of them, ``gated_layer`` and ``pruned_stack``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TokenGateError", "lib", "library_path", "TG_F32", "TG_BF16",
+    "tg_gate_score", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
+    "tg_keybias_attn", "tg_get_device_status", "gated_layer", "pruned_stack",
+    "EXPORTED_SYMBOLS",
+]
+
+TG_F32, TG_BF16 = 0, 1
+_STATUS = {0: "TG_OK", 1: "TG_ERR_INVALID_ARG", 2: "TG_ERR_UNSUPPORTED", 3: "TG_ERR_CUDA",
+           4: "TG_ERR_NAN_SCORE", 5: "TG_ERR_BAD_INDEX", 6: "TG_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libtokengate.so")
+
+_p, _i32, _i64, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+# name -> argtypes, in the order of include/tokengate.h
+_SIGNATURES = {
+    "tg_status_string": [ctypes.c_int],
+    "tg_abi_version": [],
+    "tg_last_error_message": [],
+    "tg_gate_score": [_p, ctypes.c_int, _i64, _i32, _p, _p, _i32, _p, _f32, _p, _p],
+    "tg_select_topk": [_p, _i64, _i64, _i64, _i64, _p, ctypes.POINTER(_i64), _p],
+    "tg_gather_rows": [_p, ctypes.c_int, _i64, _i32, _p, _i64, _p, ctypes.c_int, _p, _p, _p],
+    "tg_rmsnorm": [_p, ctypes.c_int, _i64, _i32, _p, _f32, _p, ctypes.c_int, _p],
+    "tg_qkv_proj": [_p, ctypes.c_int, _i64, _i32, _p, _i32, _i32, _i32, _p, _p],
+    "tg_keybias_attn": [_p, ctypes.c_int, _i64, _i32, _i32, _i32, _p, _p, _f32, _p, _p, _p],
+    "tg_get_device_status": [_p],
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lib = None
+
+
+class TokenGateError(RuntimeError):
+    def __init__(self, status: int, message: str = ""):
+        self.status = status
+        name = _STATUS.get(status, f"status {status}")
+        super().__init__(f"{name}: {message}" if message else name)
+
+
+def lib() -> ctypes.CDLL:
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(
+                f"{library_path} is missing; build it with "
+                "`python -m learned_token_pruning_residual_b300.build`")
+        L = ctypes.CDLL(library_path)
+        for name, args in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_char_p if name in ("tg_status_string", "tg_last_error_message") \
+                else ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = lib().tg_last_error_message().decode(errors="replace")
+        raise TokenGateError(status, msg)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TG_F32
+    if t.dtype == torch.bfloat16:
+        return TG_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def tg_gate_score(X, W1, b1, w2, b2: float, out=None):
+    """Gate scores [N] fp32 of the residual rows X [N][d] (bf16 or fp32)."""
+    N, d = X.shape
+    Hg = W1.shape[0]
+    if out is None:
+        out = torch.empty(N, dtype=torch.float32, device=X.device)
+    _check(lib().tg_gate_score(_ptr(X), _dt(X), N, d, _ptr(W1), _ptr(b1), Hg, _ptr(w2),
+                               float(b2), _ptr(out), _stream()))
+    return out
+
+
+def tg_select_topk(scores, doc_begin: int, doc_end: int, K: int, out=None):
+    """Ascending int32 indices of the kept tokens: all tokens outside
+    [doc_begin, doc_end) plus the K best-scoring document tokens."""
+    N = scores.shape[0]
+    M = N - (doc_end - doc_begin) + K
+    if out is None:
+        out = torch.empty(max(M, 0), dtype=torch.int32, device=scores.device)
+    m_out = _i64(0)
+    _check(lib().tg_select_topk(_ptr(scores), N, doc_begin, doc_end, K, _ptr(out),
+                                ctypes.byref(m_out), _stream()))
+    assert m_out.value == M
+    return out
+
+
+def tg_gather_rows(X, idx, scores=None, out=None, out_dtype=None, logsig_out=None):
+    """(Y, logsig): Y[m] = X[idx[m]] (idx None: identity) in out_dtype, and
+    log(sigmoid(scores[idx[m]])) when scores are given."""
+    N, d = X.shape
+    M = N if idx is None else idx.shape[0]
+    out_dtype = out_dtype or X.dtype
+    if out is None:
+        out = torch.empty(M, d, dtype=out_dtype, device=X.device)
+    if scores is not None and logsig_out is None:
+        logsig_out = torch.empty(M, dtype=torch.float32, device=X.device)
+    _check(lib().tg_gather_rows(_ptr(X), _dt(X), N, d, _ptr(idx), M, _ptr(out), _dt(out),
+                                _ptr(scores), _ptr(logsig_out) if scores is not None else None,
+                                _stream()))
+    return out, (logsig_out if scores is not None else None)
+
+
+def tg_rmsnorm(X, gamma, eps: float, out=None, out_dtype=torch.bfloat16):
+    M, d = X.shape
+    if out is None:
+        out = torch.empty(M, d, dtype=out_dtype, device=X.device)
+    _check(lib().tg_rmsnorm(_ptr(X), _dt(X), M, d, _ptr(gamma), float(eps), _ptr(out), _dt(out),
+                            _stream()))
+    return out
+
+
+def tg_qkv_proj(X, Wqkv, Hq: int, Hkv: int, dh: int, out=None):
+    M, d = X.shape
+    if out is None:
+        out = torch.empty(M, (Hq + 2 * Hkv) * dh, dtype=X.dtype, device=X.device)
+    _check(lib().tg_qkv_proj(_ptr(X), _dt(X), M, d, _ptr(Wqkv), Hq, Hkv, dh, _ptr(out), _stream()))
+    return out
+
+
+def tg_keybias_attn(QKV, Hq: int, Hkv: int, dh: int, logsig, gain, temperature: float,
+                    out=None, residual=None):
+    """O [M][Hq dh] (or residual += O in fp32 when residual is given)."""
+    M = QKV.shape[0]
+    if out is None and residual is None:
+        out = torch.empty(M, Hq * dh, dtype=QKV.dtype, device=QKV.device)
+    _check(lib().tg_keybias_attn(_ptr(QKV), _dt(QKV), M, Hq, Hkv, dh, _ptr(logsig), _ptr(gain),
+                                 float(temperature), _ptr(out), _ptr(residual), _stream()))
+    return out if residual is None else residual
+
+
+def tg_get_device_status(raise_on_error: bool = True) -> int:
+    st = lib().tg_get_device_status(_stream())
+    if raise_on_error:
+        _check(st)
+    return st
+
+
+def gated_layer(X, W1, b1, w2, b2, doc_begin, doc_end, K, Wqkv, Hq, Hkv, dh, gain, temperature,
+                bufs: dict | None = None):
+    """One gated layer: score -> select -> gather -> QKV -> key-bias
+    attention, five library calls on the current stream.  ``bufs`` may hold
+    preallocated outputs (scores, idx, Xk, logsig, qkv, out)."""
+    b = bufs or {}
+    s = tg_gate_score(X, W1, b1, w2, b2, out=b.get("scores"))
+    idx = tg_select_topk(s, doc_begin, doc_end, K, out=b.get("idx"))
+    Xk, ls = tg_gather_rows(X, idx, s, out=b.get("Xk"), logsig_out=b.get("logsig"))
+    qkv = tg_qkv_proj(Xk, Wqkv, Hq, Hkv, dh, out=b.get("qkv"))
+    O = tg_keybias_attn(qkv, Hq, Hkv, dh, ls, gain, temperature, out=b.get("out"))
+    return {"scores": s, "idx": idx, "Xk": Xk, "logsig": ls, "qkv": qkv, "O": O}
+
+
+def pruned_stack(x, layers, Hq, Hkv, dh, logsig, eps: float = 1e-6, bufs: dict | None = None):
+    """x (fp32 [M][d], updated in place) <- x + attn(qkv(RMSNorm(x))) per
+    layer; ``layers`` holds dicts with Wqkv (bf16), gamma, gain, temperature.
+    logsig None runs the layers without the bias (full prefill)."""
+    M, d = x.shape
+    b = bufs or {}
+    xn = b.get("xn") if b.get("xn") is not None else torch.empty(M, d, dtype=torch.bfloat16, device=x.device)
+    qkv = b.get("qkv") if b.get("qkv") is not None else \
+        torch.empty(M, (Hq + 2 * Hkv) * dh, dtype=torch.bfloat16, device=x.device)
+    for L in layers:
+        tg_rmsnorm(x, L["gamma"], eps, out=xn)
+        tg_qkv_proj(xn, L["Wqkv"], Hq, Hkv, dh, out=qkv)
+        tg_keybias_attn(qkv, Hq, Hkv, dh, logsig, L["gain"], L["temperature"], residual=x)
+    return x

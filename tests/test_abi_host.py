@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI: the library builds/loads, exports every
+function include/tokengate.h declares, and rejects bad arguments before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import learned_token_pruning_residual_b300 as tg
+from learned_token_pruning_residual_b300 import build as tgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tokengate.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    tgbuild.build()
+    return tg.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(tg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert L.tg_abi_version() == 1
+    names = [L.tg_status_string(i).decode() for i in range(7)]
+    assert names == ["TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
+                     "TG_ERR_NAN_SCORE", "TG_ERR_BAD_INDEX", "TG_ERR_TIMEOUT"]
+    assert L.tg_status_string(99).decode() == "TG_ERR_UNKNOWN"
+
+
+def _m():
+    return ctypes.c_int64(-1)
+
+
+def test_select_argument_errors_and_host_M(L):
+    m = _m()
+    # doc_end > N
+    assert L.tg_select_topk(None, 10, 2, 20, 1, None, ctypes.byref(m), None) == 1
+    assert b"doc_end" in L.tg_last_error_message()
+    # K > D
+    assert L.tg_select_topk(None, 10, 2, 5, 4, None, ctypes.byref(m), None) == 1
+    # negative K
+    assert L.tg_select_topk(None, 10, 2, 5, -1, None, ctypes.byref(m), None) == 1
+    # N == 0 is valid and launches nothing; M is computed on the host
+    assert L.tg_select_topk(None, 0, 0, 0, 0, None, ctypes.byref(m), None) == 0
+    assert m.value == 0
+    # nothing kept (M == 0) is valid and launches nothing
+    assert L.tg_select_topk(None, 3, 0, 3, 0, None, ctypes.byref(m), None) == 0
+    assert m.value == 0
+    # NULL pointers with work to do
+    assert L.tg_select_topk(None, 10, 2, 5, 1, None, ctypes.byref(m), None) == 1
+    assert m.value == 8                                   # 10 - 3 + 1, reported before the check
+    # misaligned pointer
+    assert L.tg_select_topk(ctypes.c_void_p(0x1004), 10, 2, 5, 1, ctypes.c_void_p(0x2000),
+                            ctypes.byref(m), None) == 1
+
+
+def test_gate_argument_errors(L):
+    p = ctypes.c_void_p(0x10000)
+    assert L.tg_gate_score(p, 7, 10, 64, p, None, 16, p, 0.0, p, None) == 1          # dtype
+    assert L.tg_gate_score(p, 1, -1, 64, p, None, 16, p, 0.0, p, None) == 1          # N
+    assert L.tg_gate_score(p, 1, 10, 64, None, None, 16, p, 0.0, p, None) == 1       # NULL W1
+    assert L.tg_gate_score(p, 1, 10, 96, p, None, 16, p, 0.0, p, None) == 2          # d % 64
+    assert L.tg_gate_score(p, 1, 10, 64, p, None, 300, p, 0.0, p, None) == 2         # Hg > 256
+    assert L.tg_gate_score(p, 1, 10, 64, p, None, 24, p, 0.0, p, None) == 2          # Hg % 16
+    assert L.tg_gate_score(None, 1, 0, 64, None, None, 16, None, 0.0, None, None) == 0  # N == 0
+
+
+def test_gather_rmsnorm_qkv_attn_argument_errors(L):
+    p = ctypes.c_void_p(0x10000)
+    # f32 -> bf16 gather is not a supported pair
+    assert L.tg_gather_rows(p, 0, 10, 64, p, 5, p, 1, None, None, None) == 2
+    # idx NULL needs M == N
+    assert L.tg_gather_rows(p, 1, 10, 64, None, 5, p, 1, None, None, None) == 1
+    # scores without logsig output
+    assert L.tg_gather_rows(p, 1, 10, 64, p, 5, p, 1, p, None, None) == 1
+    # row bytes not a multiple of 16
+    assert L.tg_gather_rows(p, 1, 10, 4, p, 5, p, 1, None, None, None) == 1
+    assert L.tg_rmsnorm(p, 0, 10, 12, p, 1e-6, p, 1, None) == 1                     # d % 8
+    assert L.tg_rmsnorm(p, 0, 10, 16, p, -1.0, p, 1, None) == 1                     # eps < 0
+    assert L.tg_qkv_proj(p, 1, 10, 100, p, 16, 8, 128, p, None) == 2                # d % 64
+    assert L.tg_keybias_attn(p, 1, 10, 16, 5, 128, None, None, 1.0, p, None, None) == 1  # Hq % Hkv
+    assert L.tg_keybias_attn(p, 1, 10, 16, 8, 64, None, None, 1.0, p, None, None) == 2   # dh != 128
+    assert L.tg_keybias_attn(p, 1, 10, 16, 16, 128, None, None, 1.0, p, None, None) == 2  # G odd
+    assert L.tg_keybias_attn(p, 1, 10, 16, 8, 128, p, None, 1.0, p, None, None) == 1     # bias, no gain
+    assert L.tg_keybias_attn(p, 1, 10, 16, 8, 128, None, None, float("nan"), p, None, None) == 1
+    assert L.tg_keybias_attn(p, 0, 10, 4, 2, 48, None, None, 1.0, p, None, None) == 2    # f32 dh
+    assert L.tg_keybias_attn(None, 1, 0, 16, 8, 128, None, None, 1.0, None, None, None) == 0
+
+
+def test_python_binding_raises_without_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("has a device")
+    x = torch.zeros(4, 64)
+    with pytest.raises(ValueError):
+        tg.tg_gate_score(x, x, None, x[0], 0.0)

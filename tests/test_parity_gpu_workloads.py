@@ -1,0 +1,180 @@
+"""GPU parity of the whole gated-prefill chain on the five workloads
+(tiny fp32; 16k, 32k sweep, 128k and the 64k 20-layer stack at Qwen3-1.7B
+shapes in bf16).  Full sizes run in the same launch configuration as the
+benchmark; where the fp64 oracle would take minutes, attention is compared
+on sampled query rows (always including the last 256 = the question)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import tg_inputs as TI
+from learned_token_pruning_residual_b300 import build as tgbuild
+import learned_token_pruning_residual_b300 as tg
+from gpu_helpers import (GATE_REL, assert_attn_close, assert_gate_close, assert_stack_close, f64,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    tgbuild.build()
+    tg.lib()
+    assert tg.tg_get_device_status(raise_on_error=False) == 0
+
+
+def _weights(w):
+    gp = TI.gate_params(w)
+    return gp, TI.qkv_weight(w), TI.attn_params(w)
+
+
+def _sample_rows(M, n, seed):
+    rng = np.random.default_rng(seed)
+    tail = np.arange(max(0, M - 256), M)
+    head = rng.choice(max(1, M - 256), size=min(n, max(1, M - 256)), replace=False)
+    return np.unique(np.concatenate([head, tail, [0]])).astype(np.int64)
+
+
+def _check_selection(gpu_idx, s_orc, b, e, K):
+    """The selection is unique for a given fp32 score vector.  The GPU reads
+    its own fp32 scores (within the gate tolerance of the oracle's), so
+    compare with the oracle's selection; if they differ, every swapped pair
+    must lie within twice the gate tolerance.  Returns the oracle's idx and
+    whether the two are equal."""
+    ref = O.select_topk(s_orc.astype(np.float32), b, e, K)
+    if np.array_equal(gpu_idx, ref):
+        return ref, True
+    rms = float(np.sqrt(np.mean(s_orc ** 2)))
+    tol = GATE_REL * np.maximum(np.abs(s_orc), rms)
+    only_gpu = np.setdiff1d(gpu_idx, ref)
+    only_orc = np.setdiff1d(ref, gpu_idx)
+    assert only_gpu.size == only_orc.size
+    assert (s_orc[only_gpu].min() + 2 * tol[only_gpu].max() >= s_orc[only_orc].max())
+    return ref, False
+
+
+def _run_chain(w, K, X, gp, Wqkv, ap, rows=None):
+    Xd = to_dev(X)
+    out = tg.gated_layer(Xd, to_dev(gp["W1"]), to_dev(gp["b1"]), to_dev(gp["w2"]), gp["b2"],
+                         w.doc_begin, w.doc_end, K, to_dev(Wqkv), w.Hq, w.Hkv, w.dh,
+                         to_dev(ap["gain"]), ap["temperature"])
+    s_orc = O.gate_score(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"])
+    assert_gate_close(f64(out["scores"]), s_orc)
+    gpu_idx = out["idx"].cpu().numpy()
+    ref_idx, same = _check_selection(gpu_idx, s_orc, w.doc_begin, w.doc_end, K)
+    if not same:  # run the GPU downstream on the oracle's selection
+        Xk, ls = tg.tg_gather_rows(Xd, to_dev(ref_idx.astype(np.int32)), out["scores"])
+        qkv = tg.tg_qkv_proj(Xk, to_dev(Wqkv), w.Hq, w.Hkv, w.dh)
+        out["O"] = tg.tg_keybias_attn(qkv, w.Hq, w.Hkv, w.dh, ls, to_dev(ap["gain"]),
+                                      ap["temperature"])
+    Xk_r, ls_r = O.gather_rows(X, ref_idx, s_orc.astype(np.float32))
+    qkv_r = O.qkv_proj(Xk_r, Wqkv)
+    O_r = O.keybias_attn(qkv_r, w.Hq, w.Hkv, w.dh, ls_r, ap["gain"], ap["temperature"], rows=rows)
+    got = f64(out["O"])
+    if rows is not None:
+        got = got[rows]
+    assert tg.tg_get_device_status(raise_on_error=False) == 0
+    return assert_attn_close(got, O_r), same
+
+
+def test_tiny_f32_gated_layer():
+    w = TI.WORKLOADS["tiny_f32_n512"]
+    X = TI.residual(w)
+    gp, Wqkv, ap = _weights(w)
+    K = w.Ks()[0]
+    out = tg.gated_layer(to_dev(X), to_dev(gp["W1"]), to_dev(gp["b1"]), to_dev(gp["w2"]),
+                         gp["b2"], w.doc_begin, w.doc_end, K, to_dev(Wqkv), w.Hq, w.Hkv, w.dh,
+                         to_dev(ap["gain"]), ap["temperature"])
+    ref = O.gated_layer(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"], w.doc_begin, w.doc_end, K,
+                        Wqkv, w.Hq, w.Hkv, w.dh, ap["gain"], ap["temperature"])
+    assert_gate_close(f64(out["scores"]), ref["scores"])
+    assert np.array_equal(out["idx"].cpu().numpy(), ref["idx"])
+    assert out["idx"].shape[0] == 192 and (out["idx"][-64:].cpu().numpy() == np.arange(448, 512)).all()
+    np.testing.assert_allclose(f64(out["qkv"]), ref["QKV"], rtol=2e-4, atol=2e-5)
+    np.testing.assert_allclose(f64(out["O"]), ref["O"], rtol=1e-4, atol=2e-5)
+
+
+def test_16k_gated_layer():
+    w = TI.WORKLOADS["qwen3_1p7b_n16k_keep10"]
+    X = TI.residual(w)
+    gp, Wqkv, ap = _weights(w)
+    (mx, mean), _ = _run_chain(w, w.Ks()[0], X, gp, Wqkv, ap)
+    print(f"16k gated layer: attention max-abs {mx:.2e} mean-abs {mean:.2e}")
+
+
+def test_32k_budget_sweep():
+    w = TI.WORKLOADS["qwen3_1p7b_n32k_sweep"]
+    X = TI.residual(w)
+    gp, Wqkv, ap = _weights(w)
+    for K in w.Ks():
+        rows = _sample_rows(w.M(K), 1024, seed=K)
+        (mx, mean), _ = _run_chain(w, K, X, gp, Wqkv, ap, rows=rows)
+        print(f"32k K={K}: attention max-abs {mx:.2e} mean-abs {mean:.2e}")
+
+
+def test_128k_gate_all_rows_and_gated_chain():
+    w = TI.WORKLOADS["qwen3_1p7b_n128k_keep6p25"]
+    X = TI.residual(w)
+    gp, Wqkv, ap = _weights(w)
+    K = w.Ks()[0]
+    rows = _sample_rows(w.M(K), 1024, seed=3)
+    (mx, mean), _ = _run_chain(w, K, X, gp, Wqkv, ap, rows=rows)
+    print(f"128k gated: attention max-abs {mx:.2e} mean-abs {mean:.2e}")
+
+
+def test_128k_full_prefill_attention_sampled_rows():
+    """Full-context attention at M = N = 131072 on the same kernel (no bias)."""
+    w = TI.WORKLOADS["qwen3_1p7b_n128k_keep6p25"]
+    M = w.N
+    QKV = TI.random_qkv(M, w.Hq, w.Hkv, w.dh, seed=77)
+    t = 1.1
+    got = tg.tg_keybias_attn(to_dev(QKV), w.Hq, w.Hkv, w.dh, None, None, t)
+    rows = _sample_rows(M, 48, seed=5)
+    ref = O.keybias_attn(QKV, w.Hq, w.Hkv, w.dh, None, np.zeros(w.Hq), t, rows=rows)
+    assert_attn_close(f64(got)[rows], ref)
+    assert tg.tg_get_device_status(raise_on_error=False) == 0
+
+
+def _stack_layers(w, n):
+    return [{"Wqkv": TI.qkv_weight(w, layer=i), "gamma": TI.rms_gamma(w, layer=i),
+             **TI.attn_params(w, layer=i)} for i in range(n)]
+
+
+def _dev_layers(layers):
+    return [{"Wqkv": to_dev(L["Wqkv"]), "gamma": to_dev(L["gamma"]), "gain": to_dev(L["gain"]),
+             "temperature": L["temperature"]} for L in layers]
+
+
+def test_64k_stack_one_layer_full_rows():
+    """One pruned layer (RMSNorm -> QKV -> key-bias attention -> residual add)
+    at the stack's kept-row count M = 6784, on generated inputs."""
+    w = TI.WORKLOADS["qwen3_1p7b_n64k_stack20_keep10"]
+    M = w.M(w.Ks()[0])
+    x0 = np.random.default_rng(8).standard_normal((M, w.d)).astype(np.float32)
+    ls = TI.random_logsig(M, seed=8)
+    layers = _stack_layers(w, 1)
+    x = to_dev(x0)
+    tg.pruned_stack(x, _dev_layers(layers), w.Hq, w.Hkv, w.dh, to_dev(ls))
+    rows = _sample_rows(M, 1024, seed=8)
+    L = layers[0]
+    qkv = O.qkv_proj(O.rmsnorm(x0, L["gamma"], 1e-6), L["Wqkv"])
+    ref = x0[rows].astype(np.float64) + O.keybias_attn(qkv, w.Hq, w.Hkv, w.dh, ls, L["gain"],
+                                                       L["temperature"], rows=rows)
+    assert_attn_close(f64(x)[rows], ref)
+
+
+def test_stack_20_layers_small_rows():
+    """All 20 layers end to end (no teacher forcing) at a reduced row count,
+    against the untethered fp64 stack.  The errors of 20 bf16 layers
+    accumulate; the bound is sqrt(20) times the attention tolerance."""
+    w = TI.WORKLOADS["qwen3_1p7b_n64k_stack20_keep10"]
+    M = 640
+    x0 = np.random.default_rng(9).standard_normal((M, w.d)).astype(np.float32)
+    ls = TI.random_logsig(M, seed=9)
+    layers = _stack_layers(w, w.layers)
+    x = to_dev(x0)
+    tg.pruned_stack(x, _dev_layers(layers), w.Hq, w.Hkv, w.dh, to_dev(ls))
+    ref = O.pruned_stack(x0, layers, w.Hq, w.Hkv, w.dh, ls)
+    mx, mean = assert_stack_close(f64(x), ref, w.layers)
+    print(f"20-layer stack: max-abs {mx:.2e} mean-abs {mean:.2e}")
