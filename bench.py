@@ -8,7 +8,7 @@ the kept rows.  Default workload: Qwen3-1.7B shapes at N = 16384 (document
 16128, question 256, 10% of the document kept).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--graph]
+                    [--impl ours|reference] [--no-graph]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own copy
 of the workload (independent prompts, no data-path collective) and the
@@ -18,6 +18,7 @@ reported value is the tokens of all ranks over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -195,6 +196,20 @@ def oracle_setup(w, K):
     return host, {"s32": s32, "qkv": O.qkv_proj(Xk, host["Wqkv"])}
 
 
+def cudart():
+    """The CUDA runtime library this process already loaded (through torch)."""
+    with open("/proc/self/maps") as f:
+        for line in f:
+            if "libcudart" in line:
+                L = ctypes.CDLL(line.split()[-1])
+                break
+        else:
+            L = ctypes.CDLL("libcudart.so")
+    L.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    L.cudaEventRecordWithFlags.restype = ctypes.c_int
+    return L
+
+
 def blas_threads() -> int:
     """Threads the oracle's BLAS calls use (its matmuls); its elementwise
     numpy steps run on one thread."""
@@ -300,7 +315,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     cur = {"sh": stream.cuda_stream}  # stream the C-ABI calls launch on
-    m_out = __import__("ctypes").c_int64(0)
+    m_out = ctypes.c_int64(0)
     t = ap["temperature"]
     ptr = {k: v.data_ptr() for k, v in dict(X=X, W1=W1, b1=b1, w2=w2, Wqkv=Wqkv, gain=gain,
                                            s=scores, idx=idx, Xk=Xk, ls=ls, qkv=qkv,
@@ -315,7 +330,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
         lambda: check(L.tg_gate_score(ptr["X"], 1, w.N, w.d, ptr["W1"], ptr["b1"], w.Hg,
                                       ptr["w2"], gp["b2"], ptr["s"], cur["sh"])),
         lambda: check(L.tg_select_topk(ptr["s"], w.N, w.doc_begin, w.doc_end, K, ptr["idx"],
-                                       __import__("ctypes").byref(m_out), cur["sh"])),
+                                       ctypes.byref(m_out), cur["sh"])),
         lambda: check(L.tg_gather_rows(ptr["X"], 1, w.N, w.d, ptr["idx"], M, ptr["Xk"], 1,
                                        ptr["s"], ptr["ls"], cur["sh"])),
         lambda: check(L.tg_qkv_proj(ptr["Xk"], 1, M, w.d, ptr["Wqkv"], w.Hq, w.Hkv, w.dh,
@@ -324,23 +339,39 @@ def run_gpu(args, w, K, rank, world, local_rank):
                                         ptr["gain"], t, ptr["out"], None, cur["sh"])),
     ]
 
-    def step(evs=None):
+    def step(evs=None, record=None):
+        rec = record or (lambda ev: ev.record(stream))
         if evs is not None:
-            evs[0].record(stream)
+            rec(evs[0])
         for i, c in enumerate(calls):
             c()
             if evs is not None:
-                evs[i + 1].record(stream)
+                rec(evs[i + 1])
 
-    graph = None
-    if args.graph:
+    nev = len(KERNELS) + 1
+    graph, gev = None, None
+    if not args.no_graph:
+        # the step as one CUDA graph, with an event-record node before and
+        # after every call so each kernel is still timed on the device
         step()  # load modules / set attributes outside capture
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
+        gev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+        for ev in gev:  # torch creates the event handle on its first record
+            ev.record(stream)
+        torch.cuda.synchronize()
+        rt = cudart()
+
+        def record_node(ev):  # cudaEventRecordExternal: a real record node in the graph
+            rc = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event),
+                                             ctypes.c_void_p(side.cuda_stream), 1)
+            if rc != 0:
+                raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
+
         cur["sh"] = side.cuda_stream
         with torch.cuda.graph(graph, stream=side):
-            step()
+            step(gev, record=record_node)
         cur["sh"] = stream.cuda_stream
     for _ in range(args.warmup):
         flush.zero_()
@@ -357,22 +388,26 @@ def run_gpu(args, w, K, rank, world, local_rank):
     sampler = ClockSampler(uuid) if rank == 0 else None
     if sampler:
         sampler.start()
-    nev = 2 if graph is not None else len(KERNELS) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    evs = None if graph is not None else \
+        [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    per = np.zeros((args.steps, len(KERNELS)))
+    step_ms = np.zeros(args.steps)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.active = True
-    torch.cuda._sleep(50_000_000)  # let the host queue run ahead of the device
+    if graph is None:
+        torch.cuda._sleep(50_000_000)  # let the host queue run ahead of the device
     for k in range(args.steps):
         flush.zero_()  # L2 flush between steps, outside the timed events
         if graph is None:
             step(evs[k])
         else:
-            evs[k][0].record(stream)
             graph.replay()
-            evs[k][1].record(stream)
+            gev[-1].synchronize()  # read this step's event nodes before the next replay
+            per[k] = [gev[i].elapsed_time(gev[i + 1]) for i in range(len(KERNELS))]
+            step_ms[k] = gev[0].elapsed_time(gev[-1])
     torch.cuda.synchronize()
     if sampler:
         sampler.active = False
@@ -383,7 +418,9 @@ def run_gpu(args, w, K, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
 
-    step_ms = np.array([e[0].elapsed_time(e[-1]) for e in evs])
+    if graph is None:
+        step_ms = np.array([e[0].elapsed_time(e[-1]) for e in evs])
+        per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(len(KERNELS))] for e in evs])
     ms_per_step = reduce_max(float(step_ms.mean()), dist, dev)
     value = aggregate_tokens_per_s(w.N, world, ms_per_step)
 
@@ -415,16 +452,12 @@ def run_gpu(args, w, K, rank, world, local_rank):
     work = algorithmic_work(w, K)
     peaks, peak_src = load_peaks()
     kernels = {}
-    if graph is None:
-        per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(len(KERNELS))] for e in evs])
-        for i, name in enumerate(KERNELS):
-            ms = float(per[:, i].mean())
-            wk = work[name]
-            kernels[name] = {"ms": ms, "GB/s": wk["bytes"] / ms / 1e6,
-                             "TFLOP/s": wk["flops"] / ms / 1e9 if wk["flops"] else None}
-        dom = max(KERNELS, key=lambda n: kernels[n]["ms"])
-    else:
-        dom = None
+    for i, name in enumerate(KERNELS):
+        ms = float(per[:, i].mean())
+        wk = work[name]
+        kernels[name] = {"ms": ms, "GB/s": wk["bytes"] / ms / 1e6,
+                         "TFLOP/s": wk["flops"] / ms / 1e9 if wk["flops"] else None}
+    dom = max(KERNELS, key=lambda n: kernels[n]["ms"])
     roofline = None
     if dom is not None:
         wk = work[dom]
@@ -450,7 +483,8 @@ def run_gpu(args, w, K, rank, world, local_rank):
                    "d_model": w.d, "gate_hidden": w.Hg, "heads_q": w.Hq, "heads_kv": w.Hkv,
                    "head_dim": w.dh, "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (256 MiB write), outside the timed events",
-                   "launch": "CUDA graph" if graph is not None else "direct C-ABI calls"},
+                   "launch": ("one CUDA graph per step (kernels timed by event-record nodes)"
+                              if graph is not None else "direct C-ABI calls")},
         "roofline": roofline,
         "attn_tflops": attn["TFLOP/s"] if attn else None,
         "attn_frac_bf16_peak": (attn["TFLOP/s"] / peaks["bf16_tflops"]) if attn else None,
@@ -477,7 +511,8 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(TI.WORKLOADS))
     ap.add_argument("--budget", type=int, default=0, help="index into the workload's budgets")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--graph", action="store_true", help="replay the step as one CUDA graph")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the five calls directly instead of replaying one CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kRowThreads)
     const uint4* src = reinterpret_cast<const uint4*>(X + (ok ? i : 0) * in_bytes);
     uint8_t* dst_row = Y + m * out_bytes;
     if (logsig != nullptr && lane == 0) logsig[m] = ok ? logsigmoid_f32(__ldg(scores + i)) : 0.f;
-    constexpr int U = 4;
+    constexpr int U = 8;  // a 2048-wide bf16 row in one round trip per lane
     for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
       uint4 buf[U];
 #pragma unroll
