@@ -16,8 +16,16 @@
 //   warp 1      one thread issues tcgen05.mma: S_t = Q_t K_j^T into TMEM
 //               (SS form), and O_t += P_t V_j with P_t read from TMEM (TS
 //               form, V MN-major).
+//   warp 2      writes each key tile's bias into one extra K = 16 block of
+//               the Q K^T product (see below).
 //   warps 4-7   softmax + epilogue of head h0 (t = 0), one query row per
 //   warps 8-11  thread, likewise for head h1 (t = 1).
+// The bias is added by the tensor core: Q_t gets two extra columns of ones
+// and K_j two extra columns holding g_h ls_c sqrt(dh) / t split into bf16
+// hi + lo, so S_t already holds q.k + g_h ls_c / scale and the softmax
+// reads nothing but TMEM.  Measured on B300, this removes a shared-memory
+// bias read and a barrier handshake from every softmax tile, which cost
+// about 30% of the kernel's time, for 1/16 more MMA work.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each; P_t (bf16
 // pairs) overwrites the first 64 columns of S_t once S_t is in registers.
 // The two heads ping-pong: while softmax t works, the tensor cores run
@@ -39,11 +47,20 @@ constexpr uint32_t kTileBytes = kBK * kDH * 2;  // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// The key bias rides in one extra K = 16 block of the Q K^T product: 128 rows
+// x 16 bf16, K-major without swizzle (8-row x 16-byte core matrices, 128 B
+// apart along K, 256 B apart along rows).
+constexpr uint32_t kXBytes = kBK * 16 * 2;  // 4 KB
+constexpr uint32_t kXLbo = 128, kXSbo = 256;
+__host__ __device__ constexpr uint32_t xblock_offset(int row, int col) {
+  return static_cast<uint32_t>((row >> 3) * 256 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
+}
 
 struct AttnArgs {
   int M, Hq, Hkv, G;
   int n_rb, pairs_per_kv;
   float scale2;  // t / sqrt(dh) * log2(e)
+  float bias_scale;  // sqrt(dh) / t: the bias in units of the q.k product
   const float* gain;
   __nv_bfloat16* O;
   float* residual;
@@ -56,10 +73,13 @@ struct AttnSmem {
   uint8_t k[2][kTileBytes];
   uint8_t v[2][kTileBytes];
   float ls[2][kBK];
+  uint8_t qx[2][kXBytes];  // per head t: ones in columns 2t, 2t+1
+  uint8_t kx[2][kXBytes];  // per stage: g_h ls_j sqrt(dh) / t as bf16 hi + lo, per head
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t ls_full[2], ls_empty[2];
+  uint64_t bias_full[2];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -75,6 +95,154 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
+}
+
+// v as a pair of bf16 (hi, lo) packed low-first, hi = RN(v), lo = RN(v - hi);
+// an infinite hi carries lo = 0.
+__device__ __forceinline__ uint32_t split_bf16(float v) {
+  const float hi = __bfloat162float(__float2bfloat16_rn(v));
+  const float lo = isinf(hi) ? 0.f : v - hi;
+  return pack_bf16x2(hi, lo);
+}
+
+// Softmax and epilogue of one head (t = 0 for warps 4-7, t = 1 for warps
+// 8-11): one query row per thread.
+template <bool BIAS>
+__device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& args, uint32_t tmem,
+                                                 int rb, int nkv, int h0, int warp, int lane,
+                                                 volatile int* abort) {
+  // --------------------------------------------------- softmax + epilogue
+  const int t = (warp - 4) >> 2;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;  // row within the block
+  const int64_t row = static_cast<int64_t>(rb) * kBQ + r;
+  const int h = h0 + t;
+  const uint64_t scale2 = f2(args.scale2, args.scale2);
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t s_tmem = tmem + t * 128 + lane_off;
+  const uint32_t o_tmem = tmem + 256 + t * 128 + lane_off;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    if (!(ok = warp_wait(smem_u32(&S.s_full[t]), j & 1, abort, args.status))) break;
+    tc_fence_after();
+    // the whole S row (128 fp32) in registers: four loads, one wait
+    uint32_t u[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + 32 * c, u[c]);
+    tmem_ld_wait();
+    // x = (q.k + g_h ls_j sqrt(dh) / t) t log2(e) / sqrt(dh): the bias came
+    // with the MMA, so this is one multiply per two columns
+    float x[kBK];
+#pragma unroll
+    for (int c = 0; c < kBK; c += 2)
+      f2_split(f2_mul(f2(__uint_as_float(u[c >> 5][c & 31]),
+                         __uint_as_float(u[c >> 5][(c + 1) & 31])),
+                      scale2),
+               x[c], x[c + 1]);
+    if (j == rb) {  // the diagonal tile: key c is row rb*128 + c
+#pragma unroll
+      for (int c = 0; c < kBK; ++c)
+        if (c > r) x[c] = -INFINITY;
+    }
+    // row max: four independent chains of three-input maxima
+    float mc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mc[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+    for (int c = 8; c < kBK; c += 8) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mc[k] = fmax3(mc[k], x[c + 2 * k], x[c + 2 * k + 1]);
+    }
+    const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+    const float m_new = fmaxf(m_run, mx);
+    const bool need = m_new > m_run + kRescaleThreshold;
+    const float m_old = m_run;
+    if (need) m_run = m_new;
+    // p = 2^(x - m_run), packed to bf16 pairs into the first 64 columns of S_t;
+    // the row sum in four independent pair accumulators
+    const uint64_t neg_m = f2(-m_run, -m_run);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = 64 * half + 2 * i;
+        float d0, d1;
+        f2_split(f2_add(f2(x[c], x[c + 1]), neg_m), d0, d1);
+        const float p0 = exp2_approx(d0), p1 = exp2_approx(d1);
+        acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32(s_tmem + 32 * half, pk);
+    }
+    tmem_st_wait();
+    float sum;
+    {
+      float a0, a1;
+      f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+      sum = a0 + a1;
+    }
+    // raise O to the new max once the previous P V is done with it
+    if (__any_sync(0xffffffffu, need) && j > 0) {
+      if (!(ok = warp_wait(smem_u32(&S.o_done[t]), (j - 1) & 1, abort, args.status))) break;
+      tc_fence_after();
+      const float f = need ? exp2_approx(m_old - m_new) : 1.f;
+      l_run *= f;
+      uint32_t w[32];
+#pragma unroll
+      for (int c0 = 0; c0 < kDH; c0 += 32) {
+        tmem_ld32(o_tmem + c0, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * f);
+        tmem_st32(o_tmem + c0, w);
+      }
+      tmem_st_wait();
+    }
+    l_run += sum;
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.p_full[t]));
+  }
+  // ------------------------------------------------------------ epilogue
+  if (ok && warp_wait(smem_u32(&S.o_done[t]), (nkv - 1) & 1, abort, args.status)) {
+    tc_fence_after();
+    const float inv = 1.f / l_run;
+    const bool row_ok = row < args.M;
+    uint32_t u[32];
+#pragma unroll 1
+    for (int c0 = 0; c0 < kDH; c0 += 32) {
+      tmem_ld32(o_tmem + c0, u);
+      tmem_ld_wait();
+      if (row_ok) {
+        if (args.residual != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(args.residual + row * args.ldo + h * kDH + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 a = dst[i];
+            a.x += __uint_as_float(u[4 * i + 0]) * inv;
+            a.y += __uint_as_float(u[4 * i + 1]) * inv;
+            a.z += __uint_as_float(u[4 * i + 2]) * inv;
+            a.w += __uint_as_float(u[4 * i + 3]) * inv;
+            dst[i] = a;
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(args.O + row * args.ldo + h * kDH + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv, __uint_as_float(u[8 * i + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv);
+            dst[i] = w;
+          }
+        }
+      }
+    }
+  }
 }
 
 template <bool BIAS>
@@ -103,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&S.v_full[s]), 1);
       mbar_init(smem_u32(&S.v_empty[s]), 1);
       mbar_init(smem_u32(&S.ls_full[s]), 1);
-      mbar_init(smem_u32(&S.ls_empty[s]), 8);  // 4 warps x 2 heads
+      mbar_init(smem_u32(&S.ls_empty[s]), 1);   // the bias warp
+      mbar_init(smem_u32(&S.bias_full[s]), 1);  // the bias warp -> the MMA thread
       mbar_init(smem_u32(&S.s_full[s]), 1);
       mbar_init(smem_u32(&S.p_full[s]), 4);
       mbar_init(smem_u32(&S.o_done[s]), 1);
@@ -120,235 +289,178 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&S.tmem_base), 512);
     tmem_relinquish();
   }
+  if (BIAS && (warp == 2 || warp == 3)) {
+    // the extra K block: zeros, and for Q_t ones in the two bias columns of head t
+    uint4* z = reinterpret_cast<uint4*>(S.qx[0]);
+    for (int i = threadIdx.x - 64; i < static_cast<int>(4 * kXBytes / 16); i += 64)
+      z[i] = make_uint4(0, 0, 0, 0);  // qx and kx are contiguous: 16 KB
+    __syncwarp();
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    for (int r = threadIdx.x - 64; r < kBQ; r += 64) {
+      *reinterpret_cast<uint32_t*>(S.qx[0] + xblock_offset(r, 0)) = 0x3F803F80u;
+      *reinterpret_cast<uint32_t*>(S.qx[1] + xblock_offset(r, 2)) = 0x3F803F80u;
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ----------------------------------------------------------- TMA
-      const int kcol = (args.Hq + hk) * kDH;
-      const int vcol = (args.Hq + args.Hkv + hk) * kDH;
-      const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by later blocks
-      mbar_arrive_expect_tx(smem_u32(&S.q_full), 2 * kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int bx = 0; bx < 2; ++bx)
-          tma_load_2d(smem_u32(S.q[t]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full),
-                      (h0 + t) * kDH + bx * 64, rb * kBQ);
-      int nk = 0, nls = 0, nv = 0;  // fills issued per ring
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status)) break;
-        mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
-        for (int bx = 0; bx < 2; ++bx)
-          tma_load_2d_hint(smem_u32(S.k[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.k_full[s]),
-                           kcol + bx * 64, j * kBK, pol);
-        ++nk;
-        if (BIAS) {
-          if (!mbar_wait(smem_u32(&S.ls_empty[s]), ph ^ 1, abort, args.status)) break;
-          mbar_arrive_expect_tx(smem_u32(&S.ls_full[s]), kBK * 4);
-          tma_load_1d(smem_u32(S.ls[s]), &tm_ls, smem_u32(&S.ls_full[s]), j * kBK);
-          ++nls;
+  // Registers: launched at 168 per thread (384 x 168 = 64512).  The control
+  // warpgroup (warps 0-3) gives back down to 120; the two softmax warpgroups,
+  // which hold a whole S row, take up to 192: 128 x 120 + 256 x 192 = 64512.
+  if (warp >= 4) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    softmax_epilogue<BIAS>(S, args, tmem, rb, nkv, h0, warp, lane, abort);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+    if (warp == 0) {
+      if (lane == 0) {
+        // ----------------------------------------------------------- TMA
+        const int kcol = (args.Hq + hk) * kDH;
+        const int vcol = (args.Hq + args.Hkv + hk) * kDH;
+        const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by later blocks
+        mbar_arrive_expect_tx(smem_u32(&S.q_full), 2 * kTileBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_2d(smem_u32(S.q[t]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full),
+                        (h0 + t) * kDH + bx * 64, rb * kBQ);
+        int nk = 0, nls = 0, nv = 0;  // fills issued per ring
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status)) break;
+          mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_2d_hint(smem_u32(S.k[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.k_full[s]),
+                             kcol + bx * 64, j * kBK, pol);
+          ++nk;
+          if (BIAS) {
+            if (!mbar_wait(smem_u32(&S.ls_empty[s]), ph ^ 1, abort, args.status)) break;
+            mbar_arrive_expect_tx(smem_u32(&S.ls_full[s]), kBK * 4);
+            tma_load_1d(smem_u32(S.ls[s]), &tm_ls, smem_u32(&S.ls_full[s]), j * kBK);
+            ++nls;
+          }
+          if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort, args.status)) break;
+          mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_2d_hint(smem_u32(S.v[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.v_full[s]),
+                             vcol + bx * 64, j * kBK, pol);
+          ++nv;
         }
-        if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort, args.status)) break;
-        mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
-        for (int bx = 0; bx < 2; ++bx)
-          tma_load_2d_hint(smem_u32(S.v[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.v_full[s]),
-                           vcol + bx * 64, j * kBK, pol);
-        ++nv;
-      }
-      // drain: every issued copy lands before the CTA may exit.  A fill that
-      // was already consumed has completed its phase, so in the normal case
-      // these waits return at once.
-      mbar_wait_drain(smem_u32(&S.q_full), 0);
-      for (int s = 0; s < 2; ++s) {
-        if (s < nk) mbar_wait_drain(smem_u32(&S.k_full[s]), (((nk - 1 - s) >> 1) & 1));
-        if (s < nls) mbar_wait_drain(smem_u32(&S.ls_full[s]), (((nls - 1 - s) >> 1) & 1));
-        if (s < nv) mbar_wait_drain(smem_u32(&S.v_full[s]), (((nv - 1 - s) >> 1) & 1));
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ----------------------------------------------------------- MMA
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
-      bool ok = mbar_wait(smem_u32(&S.q_full), 0, abort, args.status);
-      tc_fence_after();
-      for (int j = 0; ok && j <= nkv; ++j) {
-        const int s = j & 1;
-        if (j < nkv) {
-          ok = mbar_wait(smem_u32(&S.k_full[s]), (j >> 1) & 1, abort, args.status);
-          if (!ok) break;
-          tc_fence_after();
+        // drain: every issued copy lands before the CTA may exit.  A fill that
+        // was already consumed has completed its phase, so in the normal case
+        // these waits return at once.
+        mbar_wait_drain(smem_u32(&S.q_full), 0);
+        for (int s = 0; s < 2; ++s) {
+          if (s < nk) mbar_wait_drain(smem_u32(&S.k_full[s]), (((nk - 1 - s) >> 1) & 1));
+          if (s < nls) mbar_wait_drain(smem_u32(&S.ls_full[s]), (((nls - 1 - s) >> 1) & 1));
+          if (s < nv) mbar_wait_drain(smem_u32(&S.v_full[s]), (((nv - 1 - s) >> 1) & 1));
         }
-        for (int t = 0; ok && t < 2; ++t) {
-          if (j > 0) {
-            const int jp = j - 1, sp = jp & 1;
-            if (t == 0) {
-              ok = mbar_wait(smem_u32(&S.v_full[sp]), (jp >> 1) & 1, abort, args.status);
-              if (!ok) break;
-            }
-            ok = mbar_wait(smem_u32(&S.p_full[t]), jp & 1, abort, args.status);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ----------------------------------------------------------- MMA
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
+        // The issuing thread waits for the tensor pipe to take each MMA, so
+        // every instruction between two MMAs idles the pipe: all shared-memory
+        // descriptors are formed here, once.  A K step inside a tile is a
+        // constant added to the start-address field (address >> 4; the sum
+        // stays below 256 KB, so the field never carries).
+        uint64_t qd[2][kDH / 16];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int kk = 0; kk < kDH / 16; ++kk)
+            qd[t][kk] = smem_desc_sw128(smem_u32(S.q[t]) + (kk >> 2) * kHalfBytes + (kk & 3) * 32,
+                                        16, 1024);
+        const uint64_t kd0[2] = {smem_desc_sw128(smem_u32(S.k[0]), 16, 1024),
+                                 smem_desc_sw128(smem_u32(S.k[1]), 16, 1024)};
+        const uint64_t qxd[2] = {smem_desc_noswizzle(smem_u32(S.qx[0]), kXLbo, kXSbo),
+                                 smem_desc_noswizzle(smem_u32(S.qx[1]), kXLbo, kXSbo)};
+        const uint64_t kxd[2] = {smem_desc_noswizzle(smem_u32(S.kx[0]), kXLbo, kXSbo),
+                                 smem_desc_noswizzle(smem_u32(S.kx[1]), kXLbo, kXSbo)};
+        const uint64_t vd0[2] = {smem_desc_sw128(smem_u32(S.v[0]), kHalfBytes, 1024),
+                                 smem_desc_sw128(smem_u32(S.v[1]), kHalfBytes, 1024)};
+        bool ok = mbar_wait(smem_u32(&S.q_full), 0, abort, args.status);
+        tc_fence_after();
+        for (int j = 0; ok && j <= nkv; ++j) {
+          const int s = j & 1;
+          if (j < nkv) {
+            ok = mbar_wait(smem_u32(&S.k_full[s]), (j >> 1) & 1, abort, args.status);
+            if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[s]), (j >> 1) & 1, abort, args.status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t o_tmem = tmem + 256 + t * 128;
-            const uint32_t p_tmem = tmem + t * 128;
-            const uint32_t v0 = smem_u32(S.v[sp]);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_ts(o_tmem, p_tmem + kk * 8, smem_desc_sw128(v0 + kk * 2048, kHalfBytes, 1024),
-                     idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_u32(&S.o_done[t]));
-            if (t == 1) mma_commit(smem_u32(&S.v_empty[sp]));
           }
-          if (j < nkv) {
-            const uint32_t q0 = smem_u32(S.q[t]), k0 = smem_u32(S.k[s]);
-            const uint32_t s_tmem = tmem + t * 128;
+          for (int t = 0; ok && t < 2; ++t) {
+            if (j > 0) {
+              const int jp = j - 1, sp = jp & 1;
+              if (t == 0) {
+                ok = mbar_wait(smem_u32(&S.v_full[sp]), (jp >> 1) & 1, abort, args.status);
+                if (!ok) break;
+              }
+              ok = mbar_wait(smem_u32(&S.p_full[t]), jp & 1, abort, args.status);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t o_tmem = tmem + 256 + t * 128;
+              const uint32_t p_tmem = tmem + t * 128;
+              const uint64_t vd = vd0[sp];
+              mma_ts(o_tmem, p_tmem, vd, idesc_o, jp > 0 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < kDH / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-              mma_ss(s_tmem, smem_desc_sw128(q0 + off, 16, 1024),
-                     smem_desc_sw128(k0 + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+              for (int kk = 1; kk < kBK / 16; ++kk)
+                mma_ts(o_tmem, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o, 1u);
+              mma_commit(smem_u32(&S.o_done[t]));
+              if (t == 1) mma_commit(smem_u32(&S.v_empty[sp]));
             }
-            mma_commit(smem_u32(&S.s_full[t]));
+            if (j < nkv) {
+              const uint64_t kd = kd0[s];
+              const uint32_t s_tmem = tmem + t * 128;
+#pragma unroll
+              for (int kk = 0; kk < kDH / 16; ++kk)
+                mma_ss(s_tmem, qd[t][kk],
+                       kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
+                       kk > 0 ? 1u : 0u);
+              if (BIAS) mma_ss(s_tmem, qxd[t], kxd[s], idesc_s, 1u);
+              mma_commit(smem_u32(&S.s_full[t]));
+            }
           }
+          if (ok && j < nkv) mma_commit(smem_u32(&S.k_empty[s]));
         }
-        if (ok && j < nkv) mma_commit(smem_u32(&S.k_empty[s]));
+        mma_commit(smem_u32(&S.drain));
+        mbar_wait_drain(smem_u32(&S.drain), 0);
       }
-      mma_commit(smem_u32(&S.drain));
-      mbar_wait_drain(smem_u32(&S.drain), 0);
-    }
-  } else if (warp >= 4) {
-    // --------------------------------------------------- softmax + epilogue
-    const int t = (warp - 4) >> 2;
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // row within the block
-    const int64_t row = static_cast<int64_t>(rb) * kBQ + r;
-    const int h = h0 + t;
-    const float scale2 = args.scale2;
-    const float g2 = BIAS ? args.gain[h] * kLog2e : 0.f;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_tmem = tmem + t * 128 + lane_off;
-    const uint32_t o_tmem = tmem + 256 + t * 128 + lane_off;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
-      if (!(ok = warp_wait(smem_u32(&S.s_full[t]), j & 1, abort, args.status))) break;
-      if (BIAS && !(ok = warp_wait(smem_u32(&S.ls_full[s]), (j >> 1) & 1, abort, args.status)))
-        break;
-      tc_fence_after();
-      float x[kBK];
-      {
-        uint32_t u[32];
-#pragma unroll
-        for (int c0 = 0; c0 < kBK; c0 += 32) {
-          tmem_ld32(s_tmem + c0, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(u[i]);
-        }
-      }
+    } else if (warp == 2) {
       if (BIAS) {
-        const float4* lv = reinterpret_cast<const float4*>(S.ls[s]);
+        // ------------------------------------------------------------ bias
+        // Per key c of tile j and head t: v = g_t ls_c sqrt(dh) / t, split
+        // into bf16 hi + lo (|v - hi - lo| <= 2^-17 |v|), written into
+        // columns 2t, 2t+1 of the extra K block of stage s.  Q_t holds ones
+        // there, so the Q K^T product carries g_t ls_c / scale exactly as
+        // the softmax needs it.  Stage s is rewritten once the MMAs of tile
+        // j - 2 that read it are complete (k_empty).
+        const float f0 = args.gain[h0] * args.bias_scale;
+        const float f1 = args.gain[h0 + 1] * args.bias_scale;
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!warp_wait(smem_u32(&S.ls_full[s]), ph, abort, args.status)) break;
+          if (!warp_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status)) break;
+          const float4 l = reinterpret_cast<const float4*>(S.ls[s])[lane];
+          const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-        for (int c4 = 0; c4 < kBK / 4; ++c4) {
-          const float4 b = lv[c4];
-          x[4 * c4 + 0] = fmaf(x[4 * c4 + 0], scale2, g2 * b.x);
-          x[4 * c4 + 1] = fmaf(x[4 * c4 + 1], scale2, g2 * b.y);
-          x[4 * c4 + 2] = fmaf(x[4 * c4 + 2], scale2, g2 * b.z);
-          x[4 * c4 + 3] = fmaf(x[4 * c4 + 3], scale2, g2 * b.w);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&S.ls_empty[s]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBK; ++c) x[c] *= scale2;
-      }
-      if (j == rb) {  // the diagonal tile: key c is row rb*128 + c
-#pragma unroll
-        for (int c = 0; c < kBK; ++c)
-          if (c > r) x[c] = -INFINITY;
-      }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < kBK; ++c) mx = fmaxf(mx, x[c]);
-      const float m_new = fmaxf(m_run, mx);
-      const bool need = m_new > m_run + kRescaleThreshold;
-      const float m_old = m_run;
-      if (need) m_run = m_new;
-      // p = 2^(x - m_run), packed to bf16 pairs into the first 64 columns of S_t
-      float sum = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = exp2_approx(x[64 * half + 2 * i] - m_run);
-          const float p1 = exp2_approx(x[64 * half + 2 * i + 1] - m_run);
-          sum += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(s_tmem + 32 * half, pk);
-      }
-      tmem_st_wait();
-      // raise O to the new max once the previous P V is done with it
-      if (__any_sync(0xffffffffu, need) && j > 0) {
-        if (!(ok = warp_wait(smem_u32(&S.o_done[t]), (j - 1) & 1, abort, args.status))) break;
-        tc_fence_after();
-        const float f = need ? exp2_approx(m_old - m_new) : 1.f;
-        l_run *= f;
-        uint32_t u[32];
-#pragma unroll
-        for (int c0 = 0; c0 < kDH; c0 += 32) {
-          tmem_ld32(o_tmem + c0, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
-          tmem_st32(o_tmem + c0, u);
-        }
-        tmem_st_wait();
-      }
-      l_run += sum;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.p_full[t]));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && warp_wait(smem_u32(&S.o_done[t]), (nkv - 1) & 1, abort, args.status)) {
-      tc_fence_after();
-      const float inv = 1.f / l_run;
-      const bool row_ok = row < args.M;
-      uint32_t u[32];
-#pragma unroll 1
-      for (int c0 = 0; c0 < kDH; c0 += 32) {
-        tmem_ld32(o_tmem + c0, u);
-        tmem_ld_wait();
-        if (row_ok) {
-          if (args.residual != nullptr) {
-            float4* dst = reinterpret_cast<float4*>(args.residual + row * args.ldo + h * kDH + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 a = dst[i];
-              a.x += __uint_as_float(u[4 * i + 0]) * inv;
-              a.y += __uint_as_float(u[4 * i + 1]) * inv;
-              a.z += __uint_as_float(u[4 * i + 2]) * inv;
-              a.w += __uint_as_float(u[4 * i + 3]) * inv;
-              dst[i] = a;
-            }
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(args.O + row * args.ldo + h * kDH + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv, __uint_as_float(u[8 * i + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv);
-              dst[i] = w;
-            }
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * lane + i;
+            uint2 w;
+            w.x = split_bf16(f0 * lv[i]);
+            w.y = split_bf16(f1 * lv[i]);
+            *reinterpret_cast<uint2*>(S.kx[s] + xblock_offset(c, 0)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&S.ls_empty[s]));
+            mbar_arrive(smem_u32(&S.bias_full[s]));
           }
         }
       }
@@ -377,6 +489,7 @@ cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh
   a.n_rb = static_cast<int>((M + kBQ - 1) / kBQ);
   a.pairs_per_kv = a.G / 2;
   a.scale2 = temperature / sqrtf(static_cast<float>(dh)) * kLog2e;
+  a.bias_scale = sqrtf(static_cast<float>(dh)) / temperature;
   a.gain = gain;
   a.O = static_cast<__nv_bfloat16*>(O);
   a.residual = residual;
