@@ -183,7 +183,10 @@ tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d,
  *  O            [M][Hq dh] in `dtype`, or NULL when residual is given.
  *  residual     [M][Hq dh] fp32 or NULL: when given, residual += o in fp32
  *               (the layer's residual add), fused into the epilogue.
- * Limits: Hq % Hkv == 0.  TG_BF16: dh == 128 and (Hq / Hkv) even.
+ * Limits: Hq % Hkv == 0.  TG_BF16: dh == 128, (Hq / Hkv) even, and t finite
+ * and > 0 (the kernel folds the bias into the q.k product as
+ * g_h logsig_kept[j] sqrt(dh) / t, and takes row maxima of q.k; both need
+ * t > 0); other t return TG_ERR_UNSUPPORTED.
  * TG_F32: dh <= 128 and dh % 4 == 0.
  */
 tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M,

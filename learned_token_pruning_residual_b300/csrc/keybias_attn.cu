@@ -12,7 +12,7 @@
 // kv head, so every K/V tile is loaded once and used by both heads):
 //   warp 0      TMA: Q tiles of both heads once, then K_j, V_j (128 x 128
 //               bf16, 128-byte swizzle, 2-deep rings) and the bias inputs
-//               ls_j (128 fp32) per key tile j = 0 .. (causal) block index.
+//               ls_j (128 fp32) per key tile j of the CTA's key range.
 //   warp 1      one thread issues tcgen05.mma: S_t = Q_t K_j^T into TMEM
 //               (SS form), and O_t += P_t V_j with P_t read from TMEM (TS
 //               form, V MN-major).
@@ -33,6 +33,8 @@
 // than 2^8 (log2 units), so O is rescaled in TMEM rarely; the final division
 // by the row sum makes the result exact either way.  Causal tile skipping:
 // query block b only visits key tiles 0..b; only tile b is masked.
+//
+// Work units (query block, kv head pair) are launched heaviest first.
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -55,11 +57,10 @@ constexpr uint32_t kXLbo = 128, kXSbo = 256;
 __host__ __device__ constexpr uint32_t xblock_offset(int row, int col) {
   return static_cast<uint32_t>((row >> 3) * 256 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
 }
-
 struct AttnArgs {
   int M, Hq, Hkv, G;
   int n_rb, pairs_per_kv;
-  float scale2;  // t / sqrt(dh) * log2(e)
+  float scale2;      // t / sqrt(dh) * log2(e), > 0
   float bias_scale;  // sqrt(dh) / t: the bias in units of the q.k product
   const float* gain;
   __nv_bfloat16* O;
@@ -72,9 +73,9 @@ struct AttnSmem {
   uint8_t q[2][kTileBytes];
   uint8_t k[2][kTileBytes];
   uint8_t v[2][kTileBytes];
-  float ls[2][kBK];
   uint8_t qx[2][kXBytes];  // per head t: ones in columns 2t, 2t+1
   uint8_t kx[2][kXBytes];  // per stage: g_h ls_j sqrt(dh) / t as bf16 hi + lo, per head
+  float ls[2][kBK];
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
@@ -105,75 +106,104 @@ __device__ __forceinline__ uint32_t split_bf16(float v) {
   return pack_bf16x2(hi, lo);
 }
 
+// Writes 32 output columns [c0, c0 + 32) of one row: o = acc * inv, either
+// as bf16 into O or added in fp32 into the residual stream.
+__device__ __forceinline__ void store_out32(const AttnArgs& args, int64_t row, int h, int c0,
+                                            const float (&o)[32], float inv) {
+  if (args.residual != nullptr) {
+    float4* dst = reinterpret_cast<float4*>(args.residual + row * args.ldo + h * kDH + c0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 a = dst[i];
+      a.x += o[4 * i + 0] * inv;
+      a.y += o[4 * i + 1] * inv;
+      a.z += o[4 * i + 2] * inv;
+      a.w += o[4 * i + 3] * inv;
+      dst[i] = a;
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(args.O + row * args.ldo + h * kDH + c0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 w;
+      w.x = pack_bf16x2(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
+      w.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+      w.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+      w.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+      dst[i] = w;
+    }
+  }
+}
+
 // Softmax and epilogue of one head (t = 0 for warps 4-7, t = 1 for warps
-// 8-11): one query row per thread.
-template <bool BIAS>
+// 8-11): one query row per thread, over the CTA's key tiles [j0, j0 + nloc).
 __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& args, uint32_t tmem,
-                                                 int rb, int nkv, int h0, int warp, int lane,
-                                                 volatile int* abort) {
-  // --------------------------------------------------- softmax + epilogue
+                                                 int rb, int j0, int nloc, int h0, int warp,
+                                                 int lane, volatile int* abort) {
   const int t = (warp - 4) >> 2;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;  // row within the block
   const int64_t row = static_cast<int64_t>(rb) * kBQ + r;
   const int h = h0 + t;
-  const uint64_t scale2 = f2(args.scale2, args.scale2);
+  const float sc = args.scale2;
+  const uint64_t scale2 = f2(sc, sc);
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t s_tmem = tmem + t * 128 + lane_off;
   const uint32_t o_tmem = tmem + 256 + t * 128 + lane_off;
+  // running max m_run of x = S * scale2 (log2 units) and running sum l_run
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
-  for (int j = 0; j < nkv; ++j) {
-    if (!(ok = warp_wait(smem_u32(&S.s_full[t]), j & 1, abort, args.status))) break;
+  for (int i = 0; i < nloc; ++i) {
+    const int j = j0 + i;
+    if (!(ok = warp_wait(smem_u32(&S.s_full[t]), i & 1, abort, args.status))) break;
     tc_fence_after();
     // the whole S row (128 fp32) in registers: four loads, one wait
     uint32_t u[4][32];
 #pragma unroll
     for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + 32 * c, u[c]);
     tmem_ld_wait();
-    // x = (q.k + g_h ls_j sqrt(dh) / t) t log2(e) / sqrt(dh): the bias came
-    // with the MMA, so this is one multiply per two columns
-    float x[kBK];
-#pragma unroll
-    for (int c = 0; c < kBK; c += 2)
-      f2_split(f2_mul(f2(__uint_as_float(u[c >> 5][c & 31]),
-                         __uint_as_float(u[c >> 5][(c + 1) & 31])),
-                      scale2),
-               x[c], x[c + 1]);
     if (j == rb) {  // the diagonal tile: key c is row rb*128 + c
 #pragma unroll
       for (int c = 0; c < kBK; ++c)
-        if (c > r) x[c] = -INFINITY;
+        if (c > r) u[c >> 5][c & 31] = __float_as_uint(-INFINITY);
     }
-    // row max: four independent chains of three-input maxima
+    // row max of S (scale2 > 0, so it is the max of x / scale2): four
+    // independent chains of three-input maxima
     float mc[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mc[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+    for (int k = 0; k < 4; ++k)
+      mc[k] = fmaxf(__uint_as_float(u[0][2 * k]), __uint_as_float(u[0][2 * k + 1]));
 #pragma unroll
     for (int c = 8; c < kBK; c += 8) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mc[k] = fmax3(mc[k], x[c + 2 * k], x[c + 2 * k + 1]);
+      for (int k = 0; k < 4; ++k)
+        mc[k] = fmax3(mc[k], __uint_as_float(u[c >> 5][(c + 2 * k) & 31]),
+                      __uint_as_float(u[c >> 5][(c + 2 * k + 1) & 31]));
     }
-    const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+    const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
     const float m_new = fmaxf(m_run, mx);
     const bool need = m_new > m_run + kRescaleThreshold;
     const float m_old = m_run;
     if (need) m_run = m_new;
-    // p = 2^(x - m_run), packed to bf16 pairs into the first 64 columns of S_t;
-    // the row sum in four independent pair accumulators
+    // p = 2^(S scale2 - m_run): one FFMA per two columns, packed to bf16
+    // pairs into the first 64 columns of S_t; the row sum in four
+    // independent pair accumulators
     const uint64_t neg_m = f2(-m_run, -m_run);
     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int c = 64 * half + 2 * i;
+      for (int k = 0; k < 32; ++k) {
+        const int c = 64 * half + 2 * k;
         float d0, d1;
-        f2_split(f2_add(f2(x[c], x[c + 1]), neg_m), d0, d1);
+        f2_split(f2_fma(f2(__uint_as_float(u[c >> 5][c & 31]),
+                           __uint_as_float(u[c >> 5][(c + 1) & 31])),
+                        scale2, neg_m),
+                 d0, d1);
         const float p0 = exp2_approx(d0), p1 = exp2_approx(d1);
-        acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
-        pk[i] = pack_bf16x2(p0, p1);
+        acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
+        pk[k] = pack_bf16x2(p0, p1);
       }
       tmem_st32(s_tmem + 32 * half, pk);
     }
@@ -184,10 +214,9 @@ __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& ar
       f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
       sum = a0 + a1;
     }
-    // raise O to the new max once the previous P V is done with it
-    if (__any_sync(0xffffffffu, need) && j > 0) {
-      if (!(ok = warp_wait(smem_u32(&S.o_done[t]), (j - 1) & 1, abort, args.status))) break;
-      tc_fence_after();
+    // raise O to the new max; the P V of the previous tile is complete,
+    // since s_full of this tile was committed after it
+    if (__any_sync(0xffffffffu, need) && i > 0) {
       const float f = need ? exp2_approx(m_old - m_new) : 1.f;
       l_run *= f;
       uint32_t w[32];
@@ -196,7 +225,7 @@ __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& ar
         tmem_ld32(o_tmem + c0, w);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * f);
+        for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(__uint_as_float(w[k]) * f);
         tmem_st32(o_tmem + c0, w);
       }
       tmem_st_wait();
@@ -207,41 +236,22 @@ __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& ar
     if (lane == 0) mbar_arrive(smem_u32(&S.p_full[t]));
   }
   // ------------------------------------------------------------ epilogue
-  if (ok && warp_wait(smem_u32(&S.o_done[t]), (nkv - 1) & 1, abort, args.status)) {
-    tc_fence_after();
-    const float inv = 1.f / l_run;
-    const bool row_ok = row < args.M;
-    uint32_t u[32];
+  // own O complete (all of this head's MMAs are done)
+  const bool have = ok && nloc > 0 &&
+                    warp_wait(smem_u32(&S.o_done[t]), (nloc - 1) & 1, abort, args.status);
+  if (have) tc_fence_after();
+  if (!have) return;
+  const bool row_ok = row < args.M;
+  const float inv = 1.f / l_run;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kDH; c0 += 32) {
-      tmem_ld32(o_tmem + c0, u);
-      tmem_ld_wait();
-      if (row_ok) {
-        if (args.residual != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(args.residual + row * args.ldo + h * kDH + c0);
+  for (int c0 = 0; c0 < kDH; c0 += 32) {
+    uint32_t w[32];
+    tmem_ld32(o_tmem + c0, w);
+    tmem_ld_wait();
+    float o[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 a = dst[i];
-            a.x += __uint_as_float(u[4 * i + 0]) * inv;
-            a.y += __uint_as_float(u[4 * i + 1]) * inv;
-            a.z += __uint_as_float(u[4 * i + 2]) * inv;
-            a.w += __uint_as_float(u[4 * i + 3]) * inv;
-            dst[i] = a;
-          }
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(args.O + row * args.ldo + h * kDH + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv, __uint_as_float(u[8 * i + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv, __uint_as_float(u[8 * i + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv, __uint_as_float(u[8 * i + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv, __uint_as_float(u[8 * i + 7]) * inv);
-            dst[i] = w;
-          }
-        }
-      }
-    }
+    for (int k = 0; k < 32; ++k) o[k] = __uint_as_float(w[k]);
+    if (row_ok) store_out32(args, row, h, c0, o, inv);
   }
 }
 
@@ -256,12 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &S.abort;
 
   // work unit: heaviest query blocks first
+  const int unit = static_cast<int>(blockIdx.x);
   const int units_per_rb = args.Hkv * args.pairs_per_kv;
-  const int rb = args.n_rb - 1 - static_cast<int>(blockIdx.x) / units_per_rb;
-  const int rem = static_cast<int>(blockIdx.x) % units_per_rb;
+  const int rb = args.n_rb - 1 - unit / units_per_rb;
+  const int rem = unit % units_per_rb;
   const int hk = rem / args.pairs_per_kv;
   const int h0 = hk * args.G + 2 * (rem % args.pairs_per_kv);
   const int nkv = rb + 1;
+  const int j0 = 0, nloc = nkv;  // this CTA's key tiles [j0, j0 + nloc)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&S.q_full), 1);
@@ -294,11 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4* z = reinterpret_cast<uint4*>(S.qx[0]);
     for (int i = threadIdx.x - 64; i < static_cast<int>(4 * kXBytes / 16); i += 64)
       z[i] = make_uint4(0, 0, 0, 0);  // qx and kx are contiguous: 16 KB
-    __syncwarp();
     asm volatile("bar.sync 1, 64;" ::: "memory");
-    for (int r = threadIdx.x - 64; r < kBQ; r += 64) {
-      *reinterpret_cast<uint32_t*>(S.qx[0] + xblock_offset(r, 0)) = 0x3F803F80u;
-      *reinterpret_cast<uint32_t*>(S.qx[1] + xblock_offset(r, 2)) = 0x3F803F80u;
+    for (int rr = threadIdx.x - 64; rr < kBQ; rr += 64) {
+      *reinterpret_cast<uint32_t*>(S.qx[0] + xblock_offset(rr, 0)) = 0x3F803F80u;
+      *reinterpret_cast<uint32_t*>(S.qx[1] + xblock_offset(rr, 2)) = 0x3F803F80u;
     }
     fence_proxy_async_smem();
   }
@@ -307,15 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   // Registers: launched at 168 per thread (384 x 168 = 64512).  The control
-  // warpgroup (warps 0-3) gives back down to 120; the two softmax warpgroups,
-  // which hold a whole S row, take up to 192: 128 x 120 + 256 x 192 = 64512.
+  // warpgroup (warps 0-3) gives back down to 152; the two softmax warpgroups,
+  // which hold a whole S row, take up to 176: 128 x 152 + 256 x 176 = 64512.
+  // (This split compiles with the fewest spills.)
   if (warp >= 4) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
-    softmax_epilogue<BIAS>(S, args, tmem, rb, nkv, h0, warp, lane, abort);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
+    softmax_epilogue(S, args, tmem, rb, j0, nloc, h0, warp, lane, abort);
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 152;" ::: "memory");
     if (warp == 0) {
-      if (lane == 0) {
+      if (lane == 0 && nloc > 0) {
         // ----------------------------------------------------------- TMA
         const int kcol = (args.Hq + hk) * kDH;
         const int vcol = (args.Hq + args.Hkv + hk) * kDH;
@@ -326,9 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem_u32(S.q[t]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full),
                         (h0 + t) * kDH + bx * 64, rb * kBQ);
         int nk = 0, nls = 0, nv = 0;  // fills issued per ring
-        for (int j = 0; j < nkv; ++j) {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
+        for (int i = 0; i < nloc; ++i) {
+          const int j = j0 + i;
+          const int s = i & 1;
+          const uint32_t ph = (i >> 1) & 1;
           if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status)) break;
           mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
           for (int bx = 0; bx < 2; ++bx)
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 1) {
-      if (lane == 0) {
+      if (lane == 0 && nloc > 0) {
         // ----------------------------------------------------------- MMA
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
         constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
@@ -385,35 +398,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  smem_desc_sw128(smem_u32(S.v[1]), kHalfBytes, 1024)};
         bool ok = mbar_wait(smem_u32(&S.q_full), 0, abort, args.status);
         tc_fence_after();
-        for (int j = 0; ok && j <= nkv; ++j) {
-          const int s = j & 1;
-          if (j < nkv) {
-            ok = mbar_wait(smem_u32(&S.k_full[s]), (j >> 1) & 1, abort, args.status);
-            if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[s]), (j >> 1) & 1, abort, args.status);
+        for (int i = 0; ok && i <= nloc; ++i) {
+          const int s = i & 1;
+          if (i < nloc) {
+            ok = mbar_wait(smem_u32(&S.k_full[s]), (i >> 1) & 1, abort, args.status);
+            if (ok && BIAS)
+              ok = mbar_wait(smem_u32(&S.bias_full[s]), (i >> 1) & 1, abort, args.status);
             if (!ok) break;
             tc_fence_after();
           }
           for (int t = 0; ok && t < 2; ++t) {
-            if (j > 0) {
-              const int jp = j - 1, sp = jp & 1;
+            if (i > 0) {
+              const int ip = i - 1, sp = ip & 1;
               if (t == 0) {
-                ok = mbar_wait(smem_u32(&S.v_full[sp]), (jp >> 1) & 1, abort, args.status);
+                ok = mbar_wait(smem_u32(&S.v_full[sp]), (ip >> 1) & 1, abort, args.status);
                 if (!ok) break;
               }
-              ok = mbar_wait(smem_u32(&S.p_full[t]), jp & 1, abort, args.status);
+              ok = mbar_wait(smem_u32(&S.p_full[t]), ip & 1, abort, args.status);
               if (!ok) break;
               tc_fence_after();
               const uint32_t o_tmem = tmem + 256 + t * 128;
               const uint32_t p_tmem = tmem + t * 128;
               const uint64_t vd = vd0[sp];
-              mma_ts(o_tmem, p_tmem, vd, idesc_o, jp > 0 ? 1u : 0u);
+              mma_ts(o_tmem, p_tmem, vd, idesc_o, ip > 0 ? 1u : 0u);
 #pragma unroll
               for (int kk = 1; kk < kBK / 16; ++kk)
                 mma_ts(o_tmem, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o, 1u);
               mma_commit(smem_u32(&S.o_done[t]));
               if (t == 1) mma_commit(smem_u32(&S.v_empty[sp]));
             }
-            if (j < nkv) {
+            if (i < nloc) {
               const uint64_t kd = kd0[s];
               const uint32_t s_tmem = tmem + t * 128;
 #pragma unroll
@@ -425,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(smem_u32(&S.s_full[t]));
             }
           }
-          if (ok && j < nkv) mma_commit(smem_u32(&S.k_empty[s]));
+          if (ok && i < nloc) mma_commit(smem_u32(&S.k_empty[s]));
         }
         mma_commit(smem_u32(&S.drain));
         mbar_wait_drain(smem_u32(&S.drain), 0);
@@ -437,23 +451,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // into bf16 hi + lo (|v - hi - lo| <= 2^-17 |v|), written into
         // columns 2t, 2t+1 of the extra K block of stage s.  Q_t holds ones
         // there, so the Q K^T product carries g_t ls_c / scale exactly as
-        // the softmax needs it.  Stage s is rewritten once the MMAs of tile
-        // j - 2 that read it are complete (k_empty).
+        // the softmax needs it.  Stage s is rewritten once the MMAs of the
+        // tile two steps back that read it are complete (k_empty).
         const float f0 = args.gain[h0] * args.bias_scale;
         const float f1 = args.gain[h0 + 1] * args.bias_scale;
-        for (int j = 0; j < nkv; ++j) {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
+        for (int i = 0; i < nloc; ++i) {
+          const int s = i & 1;
+          const uint32_t ph = (i >> 1) & 1;
           if (!warp_wait(smem_u32(&S.ls_full[s]), ph, abort, args.status)) break;
           if (!warp_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status)) break;
           const float4 l = reinterpret_cast<const float4*>(S.ls[s])[lane];
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = 4 * lane + i;
+          for (int k = 0; k < 4; ++k) {
+            const int c = 4 * lane + k;
             uint2 w;
-            w.x = split_bf16(f0 * lv[i]);
-            w.y = split_bf16(f1 * lv[i]);
+            w.x = split_bf16(f0 * lv[k]);
+            w.y = split_bf16(f1 * lv[k]);
             *reinterpret_cast<uint2*>(S.kx[s] + xblock_offset(c, 0)) = w;
           }
           fence_proxy_async_smem();
@@ -507,17 +521,11 @@ cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh
   }
   const size_t smem = sizeof(AttnSmem) + 1024;
   const int grid = a.n_rb * Hkv * a.pairs_per_kv;
-  if (logsig != nullptr) {
-    cudaError_t err = cudaFuncSetAttribute(keybias_attn_kernel<true>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    keybias_attn_kernel<true><<<grid, kThreads, smem, stream>>>(tm_qkv, tm_ls, a);
-  } else {
-    cudaError_t err = cudaFuncSetAttribute(keybias_attn_kernel<false>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    keybias_attn_kernel<false><<<grid, kThreads, smem, stream>>>(tm_qkv, tm_ls, a);
-  }
+  auto kernel = logsig != nullptr ? keybias_attn_kernel<true> : keybias_attn_kernel<false>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, kThreads, smem, stream>>>(tm_qkv, tm_ls, a);
   return cudaGetLastError();
 }
 

@@ -268,6 +268,8 @@ tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq
   if (dtype == TG_BF16) {
     TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "attn bf16: dh must be 128");
     TG_REQUIRE((Hq / Hkv) % 2 == 0, TG_ERR_UNSUPPORTED, "attn bf16: Hq / Hkv must be even");
+    TG_REQUIRE(temperature > 0.f && temperature <= 3.0e38f, TG_ERR_UNSUPPORTED,
+               "attn bf16: temperature must be finite and > 0");
     return from_cuda(tg::launch_attn_bf16(QKV, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
                                           residual, st),
                      "attn bf16");

@@ -99,6 +99,10 @@ def test_gather_rmsnorm_qkv_attn_argument_errors(L):
     assert L.tg_keybias_attn(p, 1, 10, 16, 16, 128, None, None, 1.0, p, None, None) == 2  # G odd
     assert L.tg_keybias_attn(p, 1, 10, 16, 8, 128, p, None, 1.0, p, None, None) == 1     # bias, no gain
     assert L.tg_keybias_attn(p, 1, 10, 16, 8, 128, None, None, float("nan"), p, None, None) == 1
+    # bf16: the temperature must be finite and > 0
+    for t in (0.0, -1.1, float("inf")):
+        assert L.tg_keybias_attn(p, 1, 10, 16, 8, 128, None, None, t, p, None, None) == 2
+        assert b"temperature" in L.tg_last_error_message()
     assert L.tg_keybias_attn(p, 0, 10, 4, 2, 48, None, None, 1.0, p, None, None) == 2    # f32 dh
     assert L.tg_keybias_attn(None, 1, 0, 16, 8, 128, None, None, 1.0, None, None, None) == 0
 
