@@ -503,6 +503,138 @@ def run_gpu(args, w, K, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------------------- gated vs full ----
+def run_compare(args, w, K, rank, world, local_rank):
+    """The pages' comparison at one workload: the gated path (gate, select,
+    gather, then the pruned layers on the M kept rows) against full prefill
+    (the same layers on all N rows, no bias), on the same kernels.  A
+    one-layer workload runs one attention layer; the 20-layer workload runs
+    x <- x + attn(qkv(RMSNorm(x))) per layer on an fp32 residual stream.
+    Reports tokens/s of both and the peak device memory each path allocates
+    (inputs and weights included)."""
+    import torch
+
+    import learned_token_pruning_residual_b300 as tg
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    stack = w.layers > 1
+    M = w.M(K)
+    X_host = TI.residual(w)
+    gp = TI.gate_params(w)
+    layers_h = [{"Wqkv": TI.qkv_weight(w, layer=i), "gamma": TI.rms_gamma(w, layer=i),
+                 **TI.attn_params(w, layer=i)} for i in range(w.layers)]
+    W1, b1, w2 = to_dev(gp["W1"]), to_dev(gp["b1"]), to_dev(gp["w2"])
+    layers = [{"Wqkv": to_dev(L["Wqkv"]), "gamma": to_dev(L["gamma"]), "gain": to_dev(L["gain"]),
+               "temperature": L["temperature"]} for L in layers_h]
+    X = to_dev(X_host)
+    bf, f32 = torch.bfloat16, torch.float32
+
+    def gated_bufs():
+        b = {"scores": torch.empty(w.N, dtype=f32, device=dev),
+             "idx": torch.empty(M, dtype=torch.int32, device=dev),
+             "logsig": torch.empty(M, dtype=f32, device=dev),
+             "qkv": torch.empty(M, w.qkv_cols, dtype=bf, device=dev)}
+        if stack:
+            b["x"] = torch.empty(M, w.d, dtype=f32, device=dev)
+            b["xn"] = torch.empty(M, w.d, dtype=bf, device=dev)
+        else:
+            b["Xk"] = torch.empty(M, w.d, dtype=bf, device=dev)
+            b["out"] = torch.empty(M, w.Hq * w.dh, dtype=bf, device=dev)
+        return b
+
+    def full_bufs():
+        b = {"qkv": torch.empty(w.N, w.qkv_cols, dtype=bf, device=dev)}
+        if stack:
+            b["x"] = torch.empty(w.N, w.d, dtype=f32, device=dev)
+            b["xn"] = torch.empty(w.N, w.d, dtype=bf, device=dev)
+        else:
+            b["out"] = torch.empty(w.N, w.Hq * w.dh, dtype=bf, device=dev)
+        return b
+
+    def gated(b):
+        s = tg.tg_gate_score(X, W1, b1, w2, gp["b2"], out=b["scores"])
+        idx = tg.tg_select_topk(s, w.doc_begin, w.doc_end, K, out=b["idx"])
+        if stack:
+            tg.tg_gather_rows(X, idx, s, out=b["x"], logsig_out=b["logsig"])
+            tg.pruned_stack(b["x"], layers, w.Hq, w.Hkv, w.dh, b["logsig"],
+                            bufs={"xn": b["xn"], "qkv": b["qkv"]})
+        else:
+            L0 = layers[0]
+            Xk, ls = tg.tg_gather_rows(X, idx, s, out=b["Xk"], logsig_out=b["logsig"])
+            tg.tg_qkv_proj(Xk, L0["Wqkv"], w.Hq, w.Hkv, w.dh, out=b["qkv"])
+            tg.tg_keybias_attn(b["qkv"], w.Hq, w.Hkv, w.dh, ls, L0["gain"], L0["temperature"],
+                               out=b["out"])
+
+    def full(b):
+        if stack:
+            tg.tg_gather_rows(X, None, out=b["x"])  # widen the residual to fp32
+            tg.pruned_stack(b["x"], layers, w.Hq, w.Hkv, w.dh, None,
+                            bufs={"xn": b["xn"], "qkv": b["qkv"]})
+        else:
+            L0 = layers[0]
+            tg.tg_qkv_proj(X, L0["Wqkv"], w.Hq, w.Hkv, w.dh, out=b["qkv"])
+            tg.tg_keybias_attn(b["qkv"], w.Hq, w.Hkv, w.dh, None, None, L0["temperature"],
+                               out=b["out"])
+
+    def measure(fn, make_bufs, steps, warmup):
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        b = make_bufs()
+        for _ in range(warmup):
+            fn(b)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            e0.record()
+            fn(b)
+            e1.record()
+        torch.cuda.synchronize()
+        if tg.tg_get_device_status(raise_on_error=False) != 0:
+            raise RuntimeError("device status set")
+        ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        del b
+        return ms, peak
+
+    weights = sum(t.numel() * t.element_size() for t in [X, W1, b1, w2] +
+                  [v for L in layers for v in (L["Wqkv"], L["gamma"], L["gain"])])
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+    g_ms, g_peak = measure(gated, gated_bufs, steps, warmup)
+    f_ms, f_peak = measure(full, full_bufs, max(1, min(steps, 5)), 1)
+    attn_flops_full = 2.0 * w.N * w.N * w.dh * w.Hq * w.layers
+    line = {
+        "metric": ("20-layer pruned-stack prefill tokens/s, gated vs full" if stack else
+                   "one-layer prefill tokens/s, gated vs full-context attention"),
+        "value": w.N / (g_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": g_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "mode": "compare",
+        "config": {"workload": w.name, "N": w.N, "doc": [w.doc_begin, w.doc_end], "K": K, "M": M,
+                   "layers": w.layers, "l2": "not flushed (inputs larger than L2)"},
+        "gated": {"ms": g_ms, "tokens_per_s": w.N / (g_ms * 1e-3),
+                  "peak_mem_bytes": int(g_peak + weights)},
+        "full": {"ms": f_ms, "tokens_per_s": w.N / (f_ms * 1e-3),
+                 "peak_mem_bytes": int(f_peak + weights),
+                 "attn_tflops_incl_other_calls": attn_flops_full / (f_ms * 1e-3) / 1e12},
+        "speedup": f_ms / g_ms,
+        "mem_ratio": (f_peak + weights) / (g_peak + weights),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -514,12 +646,17 @@ def main(argv=None) -> int:
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the five calls directly instead of replaying one CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="step", choices=["step", "compare"],
+                    help="step: the timed gated-prefill step (default); compare: gated path vs "
+                         "full prefill on the same kernels, with peak device memory")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     w = TI.WORKLOADS[args.workload]
     K = w.Ks()[args.budget]
     if args.impl == "reference":
         return run_reference(args, w, K, rank, world)
+    if args.mode == "compare":
+        return run_compare(args, w, K, rank, world, local_rank)
     return run_gpu(args, w, K, rank, world, local_rank)
 
 

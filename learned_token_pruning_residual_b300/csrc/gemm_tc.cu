@@ -136,6 +136,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------ MMA issuer
+      // The issuing thread waits for the tensor pipe to take each MMA, so the
+      // shared-memory descriptors are formed once per stage; a K step of 16
+      // inside the 128-byte swizzle row is +32 bytes on the start-address
+      // field (address >> 4, no carry below 256 KB).
+      uint64_t a_desc[STAGES], b_desc[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) {
+        a_desc[s] = smem_desc_sw128(smem_u32(S.a[s]), 16, 1024);
+        b_desc[s] = smem_desc_sw128(smem_u32(S.b[s]), 16, 1024);
+      }
       uint32_t it = 0, local = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++local) {
@@ -150,12 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
+          uint64_t ad = 0, bd = 0;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_ss(d_tmem, smem_desc_sw128(a0 + k * 32, 16, 1024),
-                   smem_desc_sw128(b0 + k * 32, 16, 1024), kIdesc, (kb | k) != 0);
-          }
+          for (int q = 0; q < STAGES; ++q)
+            if (q == static_cast<int>(s)) {
+              ad = a_desc[q];
+              bd = b_desc[q];
+            }
+          mma_ss(d_tmem, ad, bd, kIdesc, kb != 0);
+#pragma unroll
+          for (int k = 1; k < BK / 16; ++k) mma_ss(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, 1u);
           mma_commit(smem_u32(&S.empty[s]));
         }
         if (ok) mma_commit(smem_u32(&S.acc_full[buf]));
