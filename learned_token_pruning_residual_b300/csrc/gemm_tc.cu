@@ -13,6 +13,15 @@
 // swizzle); one thread of warp 1 issues tcgen05.mma (M=128, N=BN, K=16)
 // into one of two TMEM accumulators; warps 2-5 drain the other accumulator
 // (one row per thread via tcgen05.ld) while the next tile accumulates.
+//
+// CTAs run in clusters of CL along M: the CL CTAs of a cluster take CL
+// consecutive M tiles with the same N tile, and each loads 1/CL of the B
+// tile and multicasts it to all of them.  A stage is refilled only after the
+// MMAs of every CTA in the cluster are done with it (their commits arrive on
+// each CTA's `empty` barrier).  Measured on B300 (N = 131072 rows): clusters
+// of two take the QKV projection from 113 to 111 us and leave the gate
+// kernel unchanged; clusters of four are slower (the cluster's CTAs must
+// free each stage together).
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -28,7 +37,8 @@ enum { EPI_STORE_BF16 = 0, EPI_GATE = 1 };
 
 struct GemmArgs {
   int M, N, K;
-  int tiles_n, num_tiles;
+  int tiles_m, tiles_n;
+  int num_super;  // groups of CL M tiles x N tiles
   __nv_bfloat16* C;  // EPI_STORE_BF16: [M][ldc]
   int64_t ldc;
   const float* b1;  // EPI_GATE: N = Hg <= BN
@@ -57,7 +67,7 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
@@ -70,12 +80,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kStageBytes = (BM + BN) * BK * 2;
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, 0, 0);
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
   volatile int* abort = &S.abort;
+  const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = static_cast<int>(blockIdx.x) / CL, ncl = static_cast<int>(gridDim.x) / CL;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&S.full[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), CL);  // one MMA commit from each CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&S.acc_full[b]), 1);
@@ -101,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_barrier();  // peers' barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   const int k_blocks = (args.K + BK - 1) / BK;
@@ -112,8 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_b = l2_policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
-        const int tm = tile / args.tiles_n, tn = tile - tm * args.tiles_n;
+      for (int st = cid; ok && st < args.num_super; st += ncl) {
+        const int tmg = st / args.tiles_n, tn = st - tmg * args.tiles_n;
+        const int tm = tmg * CL + crank;
         for (int kb = 0; kb < k_blocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1, abort, args.status)) {
@@ -123,7 +138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&S.full[s]);
           mbar_arrive_expect_tx(fb, kStageBytes);
           tma_load_2d_hint(smem_u32(S.a[s]), &tmA, fb, kb * BK, tm * BM, pol_a);
-          tma_load_2d_hint(smem_u32(S.b[s]), &tmB, fb, kb * BK, tn * BN, pol_b);
+          if (CL == 1) {
+            tma_load_2d_hint(smem_u32(S.b[s]), &tmB, fb, kb * BK, tn * BN, pol_b);
+          } else {
+            constexpr int kSlice = BN / CL;  // B rows this CTA loads for the cluster
+            tma_load_2d_multicast(smem_u32(S.b[s]) + crank * kSlice * BK * 2, &tmB, fb, kb * BK,
+                                  tn * BN + crank * kSlice, kClusterMask, pol_b);
+          }
           ++it;
         }
       }
@@ -148,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t it = 0, local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++local) {
+      for (int st = cid; ok && st < args.num_super; st += ncl, ++local) {
         const uint32_t buf = local & 1, aph = (local >> 1) & 1;
         if (!mbar_wait(smem_u32(&S.acc_empty[buf]), aph ^ 1, abort, args.status)) break;
         tc_fence_after();
@@ -170,7 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(d_tmem, ad, bd, kIdesc, kb != 0);
 #pragma unroll
           for (int k = 1; k < BK / 16; ++k) mma_ss(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, 1u);
-          mma_commit(smem_u32(&S.empty[s]));
+          if (CL == 1) {
+            mma_commit(smem_u32(&S.empty[s]));
+          } else {
+            mma_commit_multicast(smem_u32(&S.empty[s]), kClusterMask);
+          }
         }
         if (ok) mma_commit(smem_u32(&S.acc_full[buf]));
       }
@@ -183,11 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // the TMEM lane quadrant this warp may read
     const int r_in_tile = q * 32 + lane;
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
+    for (int st = cid; st < args.num_super; st += ncl, ++local) {
       const uint32_t buf = local & 1, aph = (local >> 1) & 1;
       if (!mbar_wait(smem_u32(&S.acc_full[buf]), aph, abort, args.status)) break;
       tc_fence_after();
-      const int tm = tile / args.tiles_n, tn = tile - tm * args.tiles_n;
+      const int tmg = st / args.tiles_n, tn = st - tmg * args.tiles_n;
+      const int tm = tmg * CL + crank;  // past the last M tile: every row fails row_ok
       const int64_t row = static_cast<int64_t>(tm) * BM + r_in_tile;
       const bool row_ok = row < args.M;
       const uint32_t t_row = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
@@ -244,29 +270,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // no CTA leaves while a peer may still multicast into it or commit to its barriers
+  if (CL > 1) cluster_barrier();
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int CL>
 cudaError_t launch_gemm(const void* A, const void* B, const GemmArgs& a0, cudaStream_t stream) {
   GemmArgs args = a0;
   args.tiles_n = (args.N + BN - 1) / BN;
-  const int tiles_m = (args.M + BM - 1) / BM;
-  args.num_tiles = tiles_m * args.tiles_n;
+  args.tiles_m = (args.M + BM - 1) / BM;
+  args.num_super = ((args.tiles_m + CL - 1) / CL) * args.tiles_n;
   args.status = device_status_word();
-  if (args.num_tiles == 0) return cudaSuccess;
+  if (args.tiles_m == 0 || args.tiles_n == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
   if (!make_tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, args.M,
                     static_cast<uint64_t>(args.K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, args.N,
-                    static_cast<uint64_t>(args.K) * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                    static_cast<uint64_t>(args.K) * 2, BK, BN / CL, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  auto kernel = gemm_bf16_tc_kernel<BN, STAGES, EPI>;
+  auto kernel = gemm_bf16_tc_kernel<BN, STAGES, EPI, CL>;
   const size_t smem = sizeof(GemmSmem<BN, STAGES>) + 1024;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const int grid = args.num_tiles < sm_count() ? args.num_tiles : sm_count();
-  kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, args);
+  const int max_clusters = sm_count() / CL;
+  const int clusters = args.num_super < max_clusters ? args.num_super : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 1 : 0;
+  err = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
@@ -283,8 +325,8 @@ cudaError_t launch_gate_bf16(const void* X, int64_t N, int d, const void* W1, co
   a.w2 = w2;
   a.b2 = b2;
   a.scores = scores;
-  if (Hg <= 128) return launch_gemm<128, 6, EPI_GATE>(X, W1, a, stream);
-  return launch_gemm<256, 4, EPI_GATE>(X, W1, a, stream);
+  if (Hg <= 128) return launch_gemm<128, 6, EPI_GATE, 2>(X, W1, a, stream);
+  return launch_gemm<256, 4, EPI_GATE, 2>(X, W1, a, stream);
 }
 
 cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int ncols, void* Y,
@@ -295,7 +337,7 @@ cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int 
   a.K = d;
   a.C = static_cast<__nv_bfloat16*>(Y);
   a.ldc = ncols;
-  return launch_gemm<256, 4, EPI_STORE_BF16>(X, W, a, stream);
+  return launch_gemm<256, 4, EPI_STORE_BF16, 2>(X, W, a, stream);
 }
 
 }  // namespace tg
