@@ -349,13 +349,18 @@ def run_gpu(args, w, K, rank, world, local_rank):
                 rec(evs[i + 1])
 
     nev = len(KERNELS) + 1
-    graph, gev = None, None
+    graph, graph_inst, gev = None, None, None
     if not args.no_graph:
-        # the step as one CUDA graph, with an event-record node before and
-        # after every call so each kernel is still timed on the device
+        # The step as one CUDA graph (timed by events around each replay),
+        # and a second copy with an event-record node before and after every
+        # call, replayed separately, for the per-kernel device times.  The
+        # record nodes serialise the kernels (their prologues can no longer
+        # overlap the previous kernel's tail), so they stay out of the
+        # timed step.
         step()  # load modules / set attributes outside capture
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
+        graph_inst = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         gev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
         for ev in gev:  # torch creates the event handle on its first record
@@ -371,6 +376,8 @@ def run_gpu(args, w, K, rank, world, local_rank):
 
         cur["sh"] = side.cuda_stream
         with torch.cuda.graph(graph, stream=side):
+            step()
+        with torch.cuda.graph(graph_inst, stream=side):
             step(gev, record=record_node)
         cur["sh"] = stream.cuda_stream
     for _ in range(args.warmup):
@@ -388,26 +395,22 @@ def run_gpu(args, w, K, rank, world, local_rank):
     sampler = ClockSampler(uuid) if rank == 0 else None
     if sampler:
         sampler.start()
-    evs = None if graph is not None else \
-        [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
-    per = np.zeros((args.steps, len(KERNELS)))
-    step_ms = np.zeros(args.steps)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev if graph is None else 2)]
+           for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.active = True
-    if graph is None:
-        torch.cuda._sleep(50_000_000)  # let the host queue run ahead of the device
+    torch.cuda._sleep(50_000_000)  # let the host queue run ahead of the device
     for k in range(args.steps):
         flush.zero_()  # L2 flush between steps, outside the timed events
         if graph is None:
             step(evs[k])
         else:
+            evs[k][0].record(stream)
             graph.replay()
-            gev[-1].synchronize()  # read this step's event nodes before the next replay
-            per[k] = [gev[i].elapsed_time(gev[i + 1]) for i in range(len(KERNELS))]
-            step_ms[k] = gev[0].elapsed_time(gev[-1])
+            evs[k][1].record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.active = False
@@ -417,10 +420,24 @@ def run_gpu(args, w, K, rank, world, local_rank):
     st = tg.tg_get_device_status(raise_on_error=False)
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
-
+    step_ms = np.array([e[0].elapsed_time(e[-1]) for e in evs])
     if graph is None:
-        step_ms = np.array([e[0].elapsed_time(e[-1]) for e in evs])
         per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(len(KERNELS))] for e in evs])
+    else:
+        # per-kernel device times from the instrumented copy of the step
+        n_inst = max(1, min(args.steps, 200))
+        for _ in range(3):
+            flush.zero_()
+            graph_inst.replay()
+        torch.cuda.synchronize()
+        per = np.zeros((n_inst, len(KERNELS)))
+        inst_ms = np.zeros(n_inst)
+        for k in range(n_inst):
+            flush.zero_()
+            graph_inst.replay()
+            gev[-1].synchronize()  # read this step's event nodes before the next replay
+            per[k] = [gev[i].elapsed_time(gev[i + 1]) for i in range(len(KERNELS))]
+            inst_ms[k] = gev[0].elapsed_time(gev[-1])
     ms_per_step = reduce_max(float(step_ms.mean()), dist, dev)
     value = aggregate_tokens_per_s(w.N, world, ms_per_step)
 
@@ -483,12 +500,15 @@ def run_gpu(args, w, K, rank, world, local_rank):
                    "d_model": w.d, "gate_hidden": w.Hg, "heads_q": w.Hq, "heads_kv": w.Hkv,
                    "head_dim": w.dh, "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (256 MiB write), outside the timed events",
-                   "launch": ("one CUDA graph per step (kernels timed by event-record nodes)"
+                   "launch": ("one CUDA graph per step, timed by events around each replay; "
+                              "per-kernel times from a separately replayed copy with an "
+                              "event-record node around every call"
                               if graph is not None else "direct C-ABI calls")},
         "roofline": roofline,
         "attn_tflops": attn["TFLOP/s"] if attn else None,
         "attn_frac_bf16_peak": (attn["TFLOP/s"] / peaks["bf16_tflops"]) if attn else None,
         "kernels": kernels,
+        "instrumented_ms_per_step": float(inst_ms.mean()) if graph is not None else None,
         "e2e": {"value": aggregate_tokens_per_s(w.N, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(X.numel() * 2),
                 "d2h_bytes_per_step": int(out.numel() * 2 + idx.numel() * 4)},

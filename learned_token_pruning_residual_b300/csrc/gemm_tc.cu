@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  grid_dependency_wait();  // inputs come from the previous kernel in the stream
+  allow_dependents_launch();
   if (EPI == EPI_GATE && warp >= 2) {
     for (int i = threadIdx.x - 64; i < BN; i += 32 * kEpiWarps) {
       S.b1[i] = (i < args.N && args.b1 != nullptr) ? args.b1[i] : 0.f;
@@ -295,19 +297,8 @@ cudaError_t launch_gemm(const void* A, const void* B, const GemmArgs& a0, cudaSt
   if (err != cudaSuccess) return err;
   const int max_clusters = sm_count() / CL;
   const int clusters = args.num_super < max_clusters ? args.num_super : max_clusters;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = CL > 1 ? 1 : 0;
-  err = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args);
+  err = launch_pdl(kernel, dim3(static_cast<unsigned>(clusters * CL)), dim3(kThreads), smem, stream,
+                   CL, tmA, tmB, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

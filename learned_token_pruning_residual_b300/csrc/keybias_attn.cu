@@ -301,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&S.tmem_base), 512);
     tmem_relinquish();
   }
+  grid_dependency_wait();  // QKV and ls come from the previous kernels in the stream
+  allow_dependents_launch();
   if (BIAS && (warp == 2 || warp == 3)) {
     // the extra K block: zeros, and for Q_t ones in the two bias columns of head t
     uint4* z = reinterpret_cast<uint4*>(S.qx[0]);
@@ -525,7 +527,8 @@ cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kernel<<<grid, kThreads, smem, stream>>>(tm_qkv, tm_ls, a);
+  err = launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, stream, 1u, tm_qkv, tm_ls, a);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kRowThreads)
   const int in_bytes = MODE == 1 ? d * 4 : d * 2;
   const int out_bytes = MODE == 0 ? d * 2 : d * 4;
   const int nvec = in_bytes / 16;  // 16-byte input vectors per row
+  grid_dependency_wait();  // idx, scores and X come from the previous kernels
+  allow_dependents_launch();
   for (int64_t m = warp_global; m < M; m += warps) {
     const int64_t i = idx ? static_cast<int64_t>(__ldg(idx + m)) : m;
     const bool ok = i >= 0 && i < N;
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kRowThreads)
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   const int64_t warps = static_cast<int64_t>(gridDim.x) * kRowWarps;
   const int n8 = d / 8;
+  grid_dependency_wait();
+  allow_dependents_launch();
   for (int64_t m = warp_global; m < M; m += warps) {
     float ss = 0.f;
     for (int v = lane; v < n8; v += 32) {
@@ -159,11 +163,14 @@ cudaError_t launch_gather(const void* X, int x_bf16, int64_t N, int d, const int
   const uint8_t* Xb = static_cast<const uint8_t*>(X);
   uint8_t* Yb = static_cast<uint8_t*>(Y);
   if (x_bf16 && y_bf16)
-    gather_rows_kernel<0><<<grid, kRowThreads, 0, stream>>>(Xb, N, d, idx, M, Yb, scores, logsig, st);
+    return launch_pdl(gather_rows_kernel<0>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, Xb, N, d,
+                      idx, M, Yb, scores, logsig, st);
   else if (!x_bf16 && !y_bf16)
-    gather_rows_kernel<1><<<grid, kRowThreads, 0, stream>>>(Xb, N, d, idx, M, Yb, scores, logsig, st);
+    return launch_pdl(gather_rows_kernel<1>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, Xb, N, d,
+                      idx, M, Yb, scores, logsig, st);
   else
-    gather_rows_kernel<2><<<grid, kRowThreads, 0, stream>>>(Xb, N, d, idx, M, Yb, scores, logsig, st);
+    return launch_pdl(gather_rows_kernel<2>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, Xb, N, d,
+                      idx, M, Yb, scores, logsig, st);
   return cudaGetLastError();
 }
 
@@ -172,13 +179,17 @@ cudaError_t launch_rmsnorm(const void* X, int x_bf16, int64_t M, int d, const fl
   if (M == 0) return cudaSuccess;
   const int grid = row_grid(M);
   if (x_bf16 && y_bf16)
-    rmsnorm_kernel<true, true><<<grid, kRowThreads, 0, stream>>>(X, M, d, gamma, eps, Y);
+    return launch_pdl(rmsnorm_kernel<true, true>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, X, M, d,
+                      gamma, eps, Y);
   else if (x_bf16)
-    rmsnorm_kernel<true, false><<<grid, kRowThreads, 0, stream>>>(X, M, d, gamma, eps, Y);
+    return launch_pdl(rmsnorm_kernel<true, false>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, X, M, d,
+                      gamma, eps, Y);
   else if (y_bf16)
-    rmsnorm_kernel<false, true><<<grid, kRowThreads, 0, stream>>>(X, M, d, gamma, eps, Y);
+    return launch_pdl(rmsnorm_kernel<false, true>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, X, M, d,
+                      gamma, eps, Y);
   else
-    rmsnorm_kernel<false, false><<<grid, kRowThreads, 0, stream>>>(X, M, d, gamma, eps, Y);
+    return launch_pdl(rmsnorm_kernel<false, false>, dim3(grid), dim3(kRowThreads), 0, stream, 1u, X, M, d,
+                      gamma, eps, Y);
   return cudaGetLastError();
 }
 

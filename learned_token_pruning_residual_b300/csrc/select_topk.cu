@@ -88,6 +88,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
   const int lo = min(D, rank * chunk), hi = min(D, lo + chunk);
   const int n = hi - lo;  // keys owned by this CTA: doc positions b + lo + [0, n)
   const float* src = scores + b + lo;
+  grid_dependency_wait();  // the scores come from the previous kernel in the stream
+  allow_dependents_launch();
 
   auto load_key = [&](int i) -> uint32_t {
     if constexpr (CACHED) {
@@ -240,11 +242,13 @@ cudaError_t launch_select(const float* scores, int64_t N, int64_t b, int64_t e, 
     cudaError_t err = cudaFuncSetAttribute(select_topk_kernel<true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    select_topk_kernel<true><<<kCtas, kThreads, smem, stream>>>(
-        scores, (int)N, (int)b, (int)e, (int)K, idx, status);
+    err = launch_pdl(select_topk_kernel<true>, dim3(kCtas), dim3(kThreads), smem, stream, 1u,
+                     scores, (int)N, (int)b, (int)e, (int)K, idx, status);
+    if (err != cudaSuccess) return err;
   } else {
-    select_topk_kernel<false><<<kCtas, kThreads, 0, stream>>>(scores, (int)N, (int)b, (int)e,
-                                                              (int)K, idx, status);
+    cudaError_t err = launch_pdl(select_topk_kernel<false>, dim3(kCtas), dim3(kThreads), 0,
+                                 stream, 1u, scores, (int)N, (int)b, (int)e, (int)K, idx, status);
+    if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }

@@ -337,6 +337,19 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// finishing.  It must call grid_dependency_wait() before it touches global
+// memory that the previous kernel writes or reads; that call returns once
+// the previous grid has completed and its writes are visible.  Calling
+// allow_dependents_launch() lets the next kernel in the stream be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Three-input maximum (one instruction on sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

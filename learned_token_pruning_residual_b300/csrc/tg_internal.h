@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "tokengate.h"
 
 namespace tg {
@@ -26,6 +28,36 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
                   uint32_t box_rows, CUtensorMapSwizzle swizzle);
 // 1-D tiled tensor map over a vector of `n` fp32 values, box of `box` values.
 bool make_tmap_1d_f32(CUtensorMap* map, const float* base, uint64_t n, uint32_t box);
+
+// Launches `kernel` on `stream` with programmatic stream serialization (the
+// kernel may begin its prologue while the previous kernel in the stream
+// drains; every kernel of this library waits for its predecessor with
+// griddepcontrol.wait before touching global memory), and as clusters of
+// `cluster` CTAs when cluster > 1.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- launchers (argument checking happens in the ABI layer)
 cudaError_t launch_gate_bf16(const void* X, int64_t N, int d, const void* W1, const float* b1,
