@@ -44,9 +44,24 @@ KERNEL_SOURCES = {"gate_score": "gemm_tc.cu", "select_topk": "select_topk.cu",
                   "gather_rows": "rows.cu", "qkv_proj": "gemm_tc.cu",
                   "keybias_attn": "keybias_attn.cu"}
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by kernel, with the sha256 (first 16 hex) of
-# the kernel's source at capture time; a stale hash reports null.
-NCU_TRAFFIC: dict[str, dict] = {}
+# dram__bytes_write.sum), keyed by workload/kernel, with the sha256 (first 16
+# hex) of the kernel's source at capture time; a stale hash reports null.
+NCU_TRAFFIC: dict[str, dict] = {
+    # Qwen3-1.7B shapes, N = 16384, 10% kept (profiles/*_qwen3_n16k.md)
+    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15364864 + 256,
+                                            "source_sha": "a0e1e31859229fe7"},
+    "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68192000 + 755712,
+                                          "source_sha": "57545a8ef5b3b38c"},
+    "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24445952 + 768,
+                                        "source_sha": "57545a8ef5b3b38c"},
+    "qwen3_1p7b_n16k_keep10/gather_rows": {"bytes_per_launch": 7728384,
+                                           "source_sha": "27ffa82b44661223"},
+    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 96512,
+                                           "source_sha": "462e7f03b2c3bbc4"},
+    # N = 131072, 6.25% kept (profiles/keybias_attn_qwen3_n128k.md)
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69941504 + 6977280,
+                                               "source_sha": "a0e1e31859229fe7"},
+}
 
 
 # --------------------------------------------------------------- workloads --
@@ -479,7 +494,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
     if dom is not None:
         wk = work[dom]
         ms = kernels[dom]["ms"]
-        trf = NCU_TRAFFIC.get(dom)
+        trf = NCU_TRAFFIC.get(f"{w.name}/{dom}")
         traffic = trf["bytes_per_launch"] if trf and trf.get("source_sha") == \
             source_hash(KERNEL_SOURCES[dom]) else None
         if wk["bound"] == "tensor":
