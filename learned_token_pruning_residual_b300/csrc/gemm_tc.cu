@@ -30,10 +30,13 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-
 enum { EPI_STORE_BF16 = 0, EPI_GATE = 1 };
+
+// Epilogue warps: the gate's GELU.w2 head is arithmetic-heavy, so two warps
+// share each TMEM lane quadrant there, each taking half of the columns.
+__host__ __device__ constexpr int epi_warps(int epi) { return epi == EPI_GATE ? 8 : 4; }
+__host__ __device__ constexpr int gemm_threads(int epi) { return 64 + 32 * epi_warps(epi); }
+
 
 struct GemmArgs {
   int M, N, K;
@@ -61,14 +64,30 @@ struct GemmSmem {
   int abort;
   float b1[256];
   float w2[256];
+  float part[2][BM];  // gate: partial row sums of the column half 1, per accumulator
 };
 
-__device__ __forceinline__ float gelu_erf(float z) {
-  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+// GELU(z) = z Phi(z) = 0.5 z (1 + erf(z / sqrt 2)), with erf from
+// Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26:
+//   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
+//   t = 1 / (1 + p x),  x >= 0,  |error| <= 1.5e-7.
+// 1 + erf(z / sqrt 2) is formed as 2 - q (z >= 0) or q (z < 0), q = poly * exp,
+// so the negative tail has no cancellation.
+__device__ __forceinline__ float gelu_as(float z) {
+  const float x = fabsf(z) * 0.70710678118654752f;
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
+  float poly = fmaf(t, 1.061405429f, -1.453152027f);
+  poly = fmaf(t, poly, 1.421413741f);
+  poly = fmaf(t, poly, -0.284496736f);
+  poly = fmaf(t, poly, 0.254829592f);
+  poly *= t;
+  const float q = poly * exp2_approx(-x * x * 1.4426950408889634f);
+  return 0.5f * z * (z >= 0.f ? 2.0f - q : q);
 }
 
 template <int BN, int STAGES, int EPI, int CL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(EPI), 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   using Smem = GemmSmem<BN, STAGES>;
@@ -81,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, 0, 0);
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
+  constexpr int kEpiWarps = epi_warps(EPI);
   volatile int* abort = &S.abort;
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int cid = static_cast<int>(blockIdx.x) / CL, ncl = static_cast<int>(gridDim.x) / CL;
@@ -108,12 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   grid_dependency_wait();  // inputs come from the previous kernel in the stream
   allow_dependents_launch();
-  if (EPI == EPI_GATE && warp >= 2) {
-    for (int i = threadIdx.x - 64; i < BN; i += 32 * kEpiWarps) {
-      S.b1[i] = (i < args.N && args.b1 != nullptr) ? args.b1[i] : 0.f;
-      S.w2[i] = (i < args.N) ? args.w2[i] : 0.f;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   if (CL > 1) cluster_barrier();  // peers' barriers exist before anyone signals them
@@ -209,10 +223,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quadrant this warp may read
     const int r_in_tile = q * 32 + lane;
+    const int chalf = (warp - 2) >> 2;  // gate: the half of the columns this warp reduces
+    if (EPI == EPI_GATE) {
+      for (int i = threadIdx.x - 64; i < BN; i += 32 * kEpiWarps) {
+        S.b1[i] = (i < args.N && args.b1 != nullptr) ? args.b1[i] : 0.f;
+        S.w2[i] = (i < args.N) ? args.w2[i] : 0.f;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+    }
     uint32_t local = 0;
     for (int st = cid; st < args.num_super; st += ncl, ++local) {
       const uint32_t buf = local & 1, aph = (local >> 1) & 1;
-      if (!mbar_wait(smem_u32(&S.acc_full[buf]), aph, abort, args.status)) break;
+      const bool ok_w = mbar_wait(smem_u32(&S.acc_full[buf]), aph, abort, args.status);
+      if (EPI == EPI_GATE) {
+        // the gate's epilogue warps meet at a named barrier below, so they
+        // leave the loop together or not at all
+        uint32_t any_fail;
+        asm volatile(
+            "{\n .reg .pred p, f;\n setp.eq.u32 f, %1, 0;\n"
+            " barrier.cta.red.or.pred p, 1, %2, f;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(any_fail)
+            : "r"(static_cast<uint32_t>(ok_w)), "n"(32 * kEpiWarps)
+            : "memory");
+        if (any_fail) break;
+      } else if (!ok_w) {
+        break;
+      }
       tc_fence_after();
       const int tmg = st / args.tiles_n, tn = st - tmg * args.tiles_n;
       const int tm = tmg * CL + crank;  // past the last M tile: every row fails row_ok
@@ -245,9 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // this warp's half of the columns; padded columns have w2 = 0
         float acc = 0.f;
+        const int cbeg = chalf * (BN / 2);
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
           if (c0 >= args.N) break;
           uint32_t r[32];
           tmem_ld32(t_row + c0, r);
@@ -255,10 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float z = __uint_as_float(r[i]) + S.b1[c0 + i];
-            acc = fmaf(S.w2[c0 + i], gelu_erf(z), acc);  // padded columns have w2 = 0
+            acc = fmaf(S.w2[c0 + i], gelu_as(z), acc);
           }
         }
-        if (row_ok) args.scores[row] = acc + args.b2;
+        if (chalf == 1) S.part[buf][r_in_tile] = acc;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+        if (chalf == 0 && row_ok) args.scores[row] = acc + S.part[buf][r_in_tile] + args.b2;
       }
       tc_fence_before();
       __syncwarp();
@@ -297,8 +337,8 @@ cudaError_t launch_gemm(const void* A, const void* B, const GemmArgs& a0, cudaSt
   if (err != cudaSuccess) return err;
   const int max_clusters = sm_count() / CL;
   const int clusters = args.num_super < max_clusters ? args.num_super : max_clusters;
-  err = launch_pdl(kernel, dim3(static_cast<unsigned>(clusters * CL)), dim3(kThreads), smem, stream,
-                   CL, tmA, tmB, args);
+  err = launch_pdl(kernel, dim3(static_cast<unsigned>(clusters * CL)), dim3(gemm_threads(EPI)),
+                   smem, stream, CL, tmA, tmB, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
