@@ -42,6 +42,8 @@ struct SelShared {
   uint32_t slice_total;
   uint32_t cta_gt, cta_eq;
   uint32_t found_prefix, found_krem;  // written by the owning CTA into every CTA
+  uint32_t above;                     // keys in higher-ranked CTAs' bins (this pass)
+  uint32_t gt_base, eq_base;          // kept / tied keys in lower-ranked CTAs' slices
   int nan_seen;
 };
 
@@ -164,8 +166,16 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t incl = block_inclusive_scan(merged, S.warp_a, &slice_total);
       if (tid == 0) S.slice_total = slice_total;
       cluster.sync();  // slice totals published; all remote histogram reads done
-      uint32_t above = 0;  // keys in the bins of higher-ranked CTAs
-      for (int c = rank + 1; c < kCtas; ++c) above += *cluster.map_shared_rank(&S.slice_total, c);
+      // one warp reads the eight slice totals; the block reads the sum from
+      // shared memory (one remote load per CTA instead of one per thread)
+      if (tid < 32) {
+        uint32_t v = (tid > rank && tid < kCtas) ? *cluster.map_shared_rank(&S.slice_total, tid) : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (tid == 0) S.above = v;
+      }
+      __syncthreads();
+      const uint32_t above = S.above;  // keys in the bins of higher-ranked CTAs
       if (tid < slice) {
         const uint32_t strictly_above = above + slice_total - incl;  // bins > this one
         const uint32_t at_or_above = strictly_above + merged;
@@ -207,12 +217,25 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads, 1)
     S.cta_eq = eq_tot;
   }
   cluster.sync();
-  uint32_t gt_before = gt_incl - gt, eq_before = eq_incl - eq;
-  for (int c = 0; c < rank; ++c) {
-    const SelShared* R = cluster.map_shared_rank(&S, c);
-    gt_before += R->cta_gt;
-    eq_before += R->cta_eq;
+  if (tid < 32) {  // counts of the lower-ranked CTAs, read once
+    uint32_t g = 0, q = 0;
+    if (tid < rank) {
+      const SelShared* R = cluster.map_shared_rank(&S, tid);
+      g = R->cta_gt;
+      q = R->cta_eq;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      q += __shfl_xor_sync(0xffffffffu, q, o);
+    }
+    if (tid == 0) {
+      S.gt_base = g;
+      S.eq_base = q;
+    }
   }
+  __syncthreads();
+  uint32_t gt_before = gt_incl - gt + S.gt_base, eq_before = eq_incl - eq + S.eq_base;
   for (int i = r0; i < r1; ++i) {
     const uint32_t k = load_key(i);
     const bool keep = k > T || (k == T && eq_before < k_eq);
