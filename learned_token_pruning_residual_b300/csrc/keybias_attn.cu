@@ -34,7 +34,14 @@
 // by the row sum makes the result exact either way.  Causal tile skipping:
 // query block b only visits key tiles 0..b; only tile b is masked.
 //
-// Work units (query block, kv head pair) are launched heaviest first.
+// Work units (query block, kv head pair) are launched heaviest first.  When
+// the kept sequence is short, the heaviest query blocks (the longest causal
+// rows) run as single-head units instead: two CTAs per head pair, each doing
+// one head.  Such a CTA has no second head to ping-pong with, so it does less
+// work per cycle, but each key tile takes ~0.65 of a two-head tile, which
+// shortens the critical path that sets the kernel time at small M.
+#include <algorithm>
+
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -60,6 +67,8 @@ __host__ __device__ constexpr uint32_t xblock_offset(int row, int col) {
 struct AttnArgs {
   int M, Hq, Hkv, G;
   int n_rb, pairs_per_kv;
+  int rb_single;     // query blocks >= this run as single-head units (two CTAs per head pair)
+  int n_single;      // number of single-head units (launched first)
   float scale2;      // t / sqrt(dh) * log2(e), > 0
   float bias_scale;  // sqrt(dh) / t: the bias in units of the q.k product
   const float* gain;
@@ -268,10 +277,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // work unit: heaviest query blocks first
   const int unit = static_cast<int>(blockIdx.x);
   const int units_per_rb = args.Hkv * args.pairs_per_kv;
-  const int rb = args.n_rb - 1 - unit / units_per_rb;
-  const int rem = unit % units_per_rb;
-  const int hk = rem / args.pairs_per_kv;
-  const int h0 = hk * args.G + 2 * (rem % args.pairs_per_kv);
+  int rb, h0, nh;  // query block, first q head, heads handled (1 or 2)
+  int hk;
+  if (unit < args.n_single) {
+    const int per = 2 * units_per_rb;
+    rb = args.n_rb - 1 - unit / per;
+    const int rem = unit % per;
+    hk = rem / (2 * args.pairs_per_kv);
+    h0 = hk * args.G + (rem % (2 * args.pairs_per_kv));
+    nh = 1;
+  } else {
+    const int u2 = unit - args.n_single;
+    rb = args.rb_single - 1 - u2 / units_per_rb;
+    const int rem = u2 % units_per_rb;
+    hk = rem / args.pairs_per_kv;
+    h0 = hk * args.G + 2 * (rem % args.pairs_per_kv);
+    nh = 2;
+  }
   const int nkv = rb + 1;
   const int j0 = 0, nloc = nkv;  // this CTA's key tiles [j0, j0 + nloc)
 
@@ -325,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (This split compiles with the fewest spills.)
   if (warp >= 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
-    softmax_epilogue(S, args, tmem, rb, j0, nloc, h0, warp, lane, abort);
+    if (warp < 4 + 4 * nh) softmax_epilogue(S, args, tmem, rb, j0, nloc, h0, warp, lane, abort);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 152;" ::: "memory");
     if (warp == 0) {
@@ -334,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kcol = (args.Hq + hk) * kDH;
         const int vcol = (args.Hq + args.Hkv + hk) * kDH;
         const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by later blocks
-        mbar_arrive_expect_tx(smem_u32(&S.q_full), 2 * kTileBytes);
-        for (int t = 0; t < 2; ++t)
+        mbar_arrive_expect_tx(smem_u32(&S.q_full), nh * kTileBytes);
+        for (int t = 0; t < nh; ++t)
           for (int bx = 0; bx < 2; ++bx)
             tma_load_2d(smem_u32(S.q[t]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full),
                         (h0 + t) * kDH + bx * 64, rb * kBQ);
@@ -409,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
-          for (int t = 0; ok && t < 2; ++t) {
+          for (int t = 0; ok && t < nh; ++t) {
             if (i > 0) {
               const int ip = i - 1, sp = ip & 1;
               if (t == 0) {
@@ -427,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 1; kk < kBK / 16; ++kk)
                 mma_ts(o_tmem, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o, 1u);
               mma_commit(smem_u32(&S.o_done[t]));
-              if (t == 1) mma_commit(smem_u32(&S.v_empty[sp]));
+              if (t == nh - 1) mma_commit(smem_u32(&S.v_empty[sp]));
             }
             if (i < nloc) {
               const uint64_t kd = kd0[s];
@@ -456,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the softmax needs it.  Stage s is rewritten once the MMAs of the
         // tile two steps back that read it are complete (k_empty).
         const float f0 = args.gain[h0] * args.bias_scale;
-        const float f1 = args.gain[h0 + 1] * args.bias_scale;
+        const float f1 = nh == 2 ? args.gain[h0 + 1] * args.bias_scale : 0.f;
         for (int i = 0; i < nloc; ++i) {
           const int s = i & 1;
           const uint32_t ph = (i >> 1) & 1;
@@ -522,7 +544,38 @@ cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh
     tm_ls = tm_qkv;  // unused
   }
   const size_t smem = sizeof(AttnSmem) + 1024;
-  const int grid = a.n_rb * Hkv * a.pairs_per_kv;
+  // Single-head units for the heaviest query blocks when that shortens the
+  // estimated makespan: a key tile costs 1 (two heads) or kSingle (one head),
+  // query block b has b + 1 tiles, and the kernel takes at least its longest
+  // unit and at least the total work spread over the SMs.  Only when the
+  // two-head units fit in one wave: measured on B300 (M = 3251, 4000), with
+  // more units than SMs the single-head units cost more than they save.
+  a.rb_single = a.n_rb;
+  a.n_single = 0;
+  if (a.n_rb * Hkv * a.pairs_per_kv < sm_count()) {
+    constexpr double kSingle = 0.75;  // measured flat optimum 0.6-0.85 at M = 1868
+    const int upr = Hkv * a.pairs_per_kv;
+    const int sms = sm_count();
+    double best = 1e30;
+    int best_rb = a.n_rb;
+    for (int rs = a.n_rb; rs >= 0; --rs) {
+      const int n1 = (a.n_rb - rs) * 2 * upr, n2 = rs * upr;
+      if (n1 + n2 > 2 * sms) break;  // more than two waves: balance is not the issue
+      double total = 0.0;
+      for (int b = 0; b < a.n_rb; ++b)
+        total += (b >= rs ? 2.0 * kSingle : 1.0) * (b + 1) * upr;
+      const double longest = rs < a.n_rb ? kSingle * a.n_rb : static_cast<double>(a.n_rb);
+      const double longest2 = rs > 0 ? static_cast<double>(rs) : 0.0;
+      const double est = std::max(std::max(longest, longest2), total / sms);
+      if (est < best - 1e-9) {
+        best = est;
+        best_rb = rs;
+      }
+    }
+    a.rb_single = best_rb;
+    a.n_single = (a.n_rb - best_rb) * 2 * upr;
+  }
+  const int grid = a.n_single + a.rb_single * Hkv * a.pairs_per_kv;
   auto kernel = logsig != nullptr ? keybias_attn_kernel<true> : keybias_attn_kernel<false>;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
