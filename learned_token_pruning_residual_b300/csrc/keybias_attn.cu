@@ -264,6 +264,65 @@ __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& ar
   }
 }
 
+// MMA issue loop of one CTA: NH heads (1 or 2) is a compile-time constant so
+// that the per-head descriptors stay in registers (a runtime head count made
+// them dynamically indexed and slowed every MMA issue).
+template <bool BIAS, int NH>
+__device__ __forceinline__ void mma_loop(AttnSmem& S, const AttnArgs& args, uint32_t tmem,
+                                         int nloc, const uint64_t (&qd)[2][kDH / 16],
+                                         const uint64_t (&kd0)[2], const uint64_t (&qxd)[2],
+                                         const uint64_t (&kxd)[2], const uint64_t (&vd0)[2],
+                                         volatile int* abort) {
+  constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
+  constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
+  bool ok = mbar_wait(smem_u32(&S.q_full), 0, abort, args.status);
+  tc_fence_after();
+  for (int i = 0; ok && i <= nloc; ++i) {
+    const int s = i & 1;
+    if (i < nloc) {
+      ok = mbar_wait(smem_u32(&S.k_full[s]), (i >> 1) & 1, abort, args.status);
+      if (ok && BIAS)
+        ok = mbar_wait(smem_u32(&S.bias_full[s]), (i >> 1) & 1, abort, args.status);
+      if (!ok) break;
+      tc_fence_after();
+    }
+#pragma unroll
+    for (int t = 0; ok && t < NH; ++t) {
+      if (i > 0) {
+        const int ip = i - 1, sp = ip & 1;
+        if (t == 0) {
+          ok = mbar_wait(smem_u32(&S.v_full[sp]), (ip >> 1) & 1, abort, args.status);
+          if (!ok) break;
+        }
+        ok = mbar_wait(smem_u32(&S.p_full[t]), ip & 1, abort, args.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t o_tmem = tmem + 256 + t * 128;
+        const uint32_t p_tmem = tmem + t * 128;
+        const uint64_t vd = vd0[sp];
+        mma_ts(o_tmem, p_tmem, vd, idesc_o, ip > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 1; kk < kBK / 16; ++kk)
+          mma_ts(o_tmem, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o, 1u);
+        mma_commit(smem_u32(&S.o_done[t]));
+        if (t == NH - 1) mma_commit(smem_u32(&S.v_empty[sp]));
+      }
+      if (i < nloc) {
+        const uint64_t kd = kd0[s];
+        const uint32_t s_tmem = tmem + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < kDH / 16; ++kk)
+          mma_ss(s_tmem, qd[t][kk],
+                 kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        if (BIAS) mma_ss(s_tmem, qxd[t], kxd[s], idesc_s, 1u);
+        mma_commit(smem_u32(&S.s_full[t]));
+      }
+    }
+    if (ok && i < nloc) mma_commit(smem_u32(&S.k_empty[s]));
+  }
+}
+
 template <bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
     keybias_attn_kernel(const __grid_constant__ CUtensorMap tm_qkv,
@@ -398,8 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       if (lane == 0 && nloc > 0) {
         // ----------------------------------------------------------- MMA
-        constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
         // The issuing thread waits for the tensor pipe to take each MMA, so
         // every instruction between two MMAs idles the pipe: all shared-memory
         // descriptors are formed here, once.  A K step inside a tile is a
@@ -420,50 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  smem_desc_noswizzle(smem_u32(S.kx[1]), kXLbo, kXSbo)};
         const uint64_t vd0[2] = {smem_desc_sw128(smem_u32(S.v[0]), kHalfBytes, 1024),
                                  smem_desc_sw128(smem_u32(S.v[1]), kHalfBytes, 1024)};
-        bool ok = mbar_wait(smem_u32(&S.q_full), 0, abort, args.status);
-        tc_fence_after();
-        for (int i = 0; ok && i <= nloc; ++i) {
-          const int s = i & 1;
-          if (i < nloc) {
-            ok = mbar_wait(smem_u32(&S.k_full[s]), (i >> 1) & 1, abort, args.status);
-            if (ok && BIAS)
-              ok = mbar_wait(smem_u32(&S.bias_full[s]), (i >> 1) & 1, abort, args.status);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          for (int t = 0; ok && t < nh; ++t) {
-            if (i > 0) {
-              const int ip = i - 1, sp = ip & 1;
-              if (t == 0) {
-                ok = mbar_wait(smem_u32(&S.v_full[sp]), (ip >> 1) & 1, abort, args.status);
-                if (!ok) break;
-              }
-              ok = mbar_wait(smem_u32(&S.p_full[t]), ip & 1, abort, args.status);
-              if (!ok) break;
-              tc_fence_after();
-              const uint32_t o_tmem = tmem + 256 + t * 128;
-              const uint32_t p_tmem = tmem + t * 128;
-              const uint64_t vd = vd0[sp];
-              mma_ts(o_tmem, p_tmem, vd, idesc_o, ip > 0 ? 1u : 0u);
-#pragma unroll
-              for (int kk = 1; kk < kBK / 16; ++kk)
-                mma_ts(o_tmem, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o, 1u);
-              mma_commit(smem_u32(&S.o_done[t]));
-              if (t == nh - 1) mma_commit(smem_u32(&S.v_empty[sp]));
-            }
-            if (i < nloc) {
-              const uint64_t kd = kd0[s];
-              const uint32_t s_tmem = tmem + t * 128;
-#pragma unroll
-              for (int kk = 0; kk < kDH / 16; ++kk)
-                mma_ss(s_tmem, qd[t][kk],
-                       kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
-                       kk > 0 ? 1u : 0u);
-              if (BIAS) mma_ss(s_tmem, qxd[t], kxd[s], idesc_s, 1u);
-              mma_commit(smem_u32(&S.s_full[t]));
-            }
-          }
-          if (ok && i < nloc) mma_commit(smem_u32(&S.k_empty[s]));
+        if (nh == 2) {
+          mma_loop<BIAS, 2>(S, args, tmem, nloc, qd, kd0, qxd, kxd, vd0, abort);
+        } else {
+          mma_loop<BIAS, 1>(S, args, tmem, nloc, qd, kd0, qxd, kxd, vd0, abort);
         }
         mma_commit(smem_u32(&S.drain));
         mbar_wait_drain(smem_u32(&S.drain), 0);
