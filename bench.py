@@ -48,8 +48,8 @@ KERNEL_SOURCES = {"gate_score": "gemm_tc.cu", "select_topk": "select_topk.cu",
 # hex) of the kernel's source at capture time; a stale hash reports null.
 NCU_TRAFFIC: dict[str, dict] = {
     # Qwen3-1.7B shapes, N = 16384, 10% kept (profiles/*_qwen3_n16k.md)
-    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15369984 + 1024,
-                                            "source_sha": "2ea0f0461d8de60d"},
+    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15378432 + 2048,
+                                            "source_sha": "3b72f3aa1585c90c"},
     "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68187904 + 627456,
                                           "source_sha": "25e1c47fd2f58bc2"},
     "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24447744 + 512,
@@ -59,8 +59,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 92672,
                                            "source_sha": "eab745ed225e14e2"},
     # N = 131072, 6.25% kept (profiles/keybias_attn_qwen3_n128k.md, gemm_gate_qkv_qwen3_n16k.md)
-    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69871872 + 7022336,
-                                               "source_sha": "2ea0f0461d8de60d"},
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69799680 + 6919168,
+                                               "source_sha": "3b72f3aa1585c90c"},
     "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537969920 + 3190016,
                                              "source_sha": "25e1c47fd2f58bc2"},
     "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51378432 + 24764416,
