@@ -12,6 +12,11 @@ Parity status per function (see the pins in ``tests/test_oracle_pins.py``):
 * rmsnorm, qkv_proj       pinned (invariants, identity weight, brute-force loops)
 * keybias_attn            pinned (SDPA special case, 2-key closed form, invariants)
 * gated_layer, stack      composed of the pinned functions above
+* keybias_attn_lse        pinned (q = 0 closed form, torch.logsumexp, row 0)
+* keybias_attn_bias_grad,
+  bias_grad_reduce        pinned (central differences of the forward, torch
+                          SDPA autograd, 2-key closed form, shift invariance)
+* attn_delta              pinned (brute-force loops, softmax written out)
 * the *learned* behaviour of a trained gate (which tokens it keeps on real
   text): parity unpinned, there are no trained weights or datasets here.
 """

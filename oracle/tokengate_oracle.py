@@ -37,6 +37,11 @@ What they leave open, and the reading taken here (one line each):
   token).
 * a pruned layer of the stack: x <- x + attn(qkv(RMSNorm(x))) (no RoPE, no
   o-proj, no MLP).
+* the gradient the bias carries back to the scorer ([DE] "Was ist
+  token-gated Attention?": the bias gives the gradient a way back to the
+  scorer; [TH] the same, MoE-router style): the plain chain rule through
+  the logit form above, with the scorer's output s_j entering only through
+  ls_j = log(sigmoid(s_j)) of the kept keys.
 
 Everything runs in float64 on values widened exactly from their stored
 formats.  numpy's matmul, sort and erf are used as library primitives; there
@@ -54,6 +59,7 @@ __all__ = [
     "score_key", "select_topk", "select_topk_by_rank", "SelectNaNError",
     "logsigmoid", "gather_rows", "rmsnorm", "qkv_proj", "split_qkv",
     "keybias_attn", "gated_layer", "pruned_stack",
+    "keybias_attn_lse", "attn_delta", "keybias_attn_bias_grad", "bias_grad_reduce",
 ]
 
 
@@ -281,3 +287,106 @@ def pruned_stack(x0, layers, Hq, Hkv, dh, logsig_kept, eps: float = 1e-6):
         qkv = qkv_proj(xn, L["Wqkv"])
         x = x + keybias_attn(qkv, Hq, Hkv, dh, logsig_kept, L["gain"], L["temperature"])
     return x
+
+
+# --------------------------------------------------------------------------
+# the gradient path to the scorer ([DE] "Was ist token-gated Attention?":
+# the kept tokens' scores become a bias on the attention logits, which gives
+# the gradient a way back to the scorer; [TH] token-gated attention, the
+# MoE-router device; [RU] "Механизм token-gated attention")
+#
+# With b_hj = g_h ls_j the bias of key j in head h, l_ij = t q_i.k_j/sqrt(dh)
+# + b_hj, P = softmax_j(l), o_i = sum_j P_ij v_j and an upstream gradient
+# dO, the chain rule gives
+#   dP_ij = dO_i . v_j,   D_i = sum_j P_ij dP_ij,   dl_ij = P_ij (dP_ij - D_i)
+#   dL/db_hj = sum_{i >= j} dl_ij      (b_hj enters every row i >= j)
+#   dL/dls_j = sum_h g_h dL/db_hj,     dL/dg_h = sum_j ls_j dL/db_hj
+#   dL/ds_j  = dL/dls_j * sigmoid(-s_j)  (d log sigmoid(s) / ds)
+# --------------------------------------------------------------------------
+def _head_logits(q, k, r, ls, g_h: float, t: float, dh: int) -> np.ndarray:
+    """l_ij for query rows r against keys [0, max(r)], -inf where j > i."""
+    jmax = int(r.max()) + 1
+    logits = t * (q[r] @ k[:jmax].T) / math.sqrt(dh)
+    if ls is not None:
+        logits = logits + g_h * ls[None, :jmax]
+    causal = np.arange(jmax)[None, :] <= r[:, None]
+    return np.where(causal, logits, -np.inf)
+
+
+def keybias_attn_lse(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain, temperature: float,
+                     chunk: int = 512) -> np.ndarray:
+    """lse[h][i] = log sum_{j <= i} exp(l_ij), natural log, float64 [Hq][M]:
+    the per-row normaliser of the softmax that the backward re-uses."""
+    Q = _widen(QKV)
+    M = Q.shape[0]
+    G = Hq // Hkv
+    q_all, k_all, _ = split_qkv(Q, Hq, Hkv, dh)
+    ls = None if logsig_kept is None else np.asarray(logsig_kept, dtype=np.float64)
+    g = np.asarray(gain, dtype=np.float64)
+    lse = np.zeros((Hq, M), dtype=np.float64)
+    for h in range(Hq):
+        hk = h // G
+        q = q_all[:, h * dh:(h + 1) * dh]
+        k = k_all[:, hk * dh:(hk + 1) * dh]
+        for c0 in range(0, M, chunk):
+            r = np.arange(c0, min(M, c0 + chunk))
+            logits = _head_logits(q, k, r, ls, g[h], float(temperature), dh)
+            mx = logits.max(axis=1, keepdims=True)
+            lse[h, r] = mx[:, 0] + np.log(np.exp(logits - mx).sum(axis=1))
+    return lse
+
+
+def attn_delta(dO, O_out, Hq: int, dh: int) -> np.ndarray:
+    """D[h][i] = dO_i^h . o_i^h over the dh columns of head h, float64 [Hq][M]
+    (equal to sum_j P_ij dP_ij when o is the exact attention output)."""
+    a = _widen(dO)
+    b = _widen(O_out)
+    M = a.shape[0]
+    return (a * b).reshape(M, Hq, dh).sum(axis=2).T.copy()
+
+
+def keybias_attn_bias_grad(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain,
+                           temperature: float, dO, chunk: int = 256) -> np.ndarray:
+    """dL/db_hj = sum_{i >= j} P_ij (dP_ij - D_i) for every head h and kept
+    key j, float64 [Hq][M], with P recomputed from the logits, dP_ij =
+    dO_i . v_j and D_i = sum_j P_ij dP_ij (its definition, not dO_i . o_i).
+    ``logsig_kept`` None means b = 0 (the gradient is still defined)."""
+    Q = _widen(QKV)
+    dOw = _widen(dO)
+    M = Q.shape[0]
+    G = Hq // Hkv
+    q_all, k_all, v_all = split_qkv(Q, Hq, Hkv, dh)
+    ls = None if logsig_kept is None else np.asarray(logsig_kept, dtype=np.float64)
+    g = np.asarray(gain, dtype=np.float64)
+    dB = np.zeros((Hq, M), dtype=np.float64)
+    for h in range(Hq):
+        hk = h // G
+        q = q_all[:, h * dh:(h + 1) * dh]
+        k = k_all[:, hk * dh:(hk + 1) * dh]
+        v = v_all[:, hk * dh:(hk + 1) * dh]
+        do = dOw[:, h * dh:(h + 1) * dh]
+        for c0 in range(0, M, chunk):
+            r = np.arange(c0, min(M, c0 + chunk))
+            logits = _head_logits(q, k, r, ls, g[h], float(temperature), dh)
+            jmax = logits.shape[1]
+            mx = logits.max(axis=1, keepdims=True)
+            p = np.exp(logits - mx)
+            p = p / p.sum(axis=1, keepdims=True)
+            dp = do[r] @ v[:jmax].T
+            D = (p * dp).sum(axis=1, keepdims=True)
+            dB[h, :jmax] += (p * (dp - D)).sum(axis=0)
+    return dB
+
+
+def bias_grad_reduce(dbias, logsig_kept, gain):
+    """From dL/db [Hq][M]: dL/dls_j = sum_h g_h dL/db_hj, dL/dg_h = sum_j ls_j
+    dL/db_hj, and dL/ds_j = dL/dls_j * sigmoid(-s_j) where ls_j = log
+    sigmoid(s_j), so sigmoid(-s_j) = 1 - exp(ls_j) = -expm1(ls_j).  Returns
+    (dls [M], dgain [Hq], ds [M]), float64."""
+    dB = np.asarray(dbias, dtype=np.float64)
+    ls = np.asarray(logsig_kept, dtype=np.float64)
+    g = np.asarray(gain, dtype=np.float64)
+    dls = g @ dB
+    dgain = dB @ ls
+    ds = dls * -np.expm1(ls)
+    return dls, dgain, ds

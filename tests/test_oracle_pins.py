@@ -401,3 +401,195 @@ def test_pruned_stack_zero_layers_and_zero_weights():
     L = {"Wqkv": np.zeros((32, 16), np.float32), "gamma": np.ones(16, np.float32),
          "gain": np.ones(4), "temperature": 1.0}
     np.testing.assert_array_equal(O.pruned_stack(x, [L, L], 4, 2, 4, None), x.astype(np.float64))
+
+
+# ------------------------------------------- the gradient path to the scorer ---
+def _loss(QKV, Hq, Hkv, dh, ls, g, t, dO):
+    return float((O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, t) * dO).sum())
+
+
+def test_bias_grad_matches_central_differences():
+    # L = sum(dO * O): dL/dls_j and dL/dg_h by central differences of the
+    # (separately pinned) forward, against the chain-rule backward
+    Hq, Hkv, dh, M, t = 4, 2, 8, 21, 1.1
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=31)
+    rng = np.random.default_rng(32)
+    ls = -rng.exponential(0.8, M)
+    g = rng.uniform(0.5, 1.5, Hq)
+    dO = rng.standard_normal((M, Hq * dh))
+    dB = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO, chunk=8)
+    dls, dgain, _ = O.bias_grad_reduce(dB, ls, g)
+    eps = 1e-6
+    fd_ls = np.zeros(M)
+    for j in range(M):
+        e = np.zeros(M)
+        e[j] = eps
+        fd_ls[j] = (_loss(QKV, Hq, Hkv, dh, ls + e, g, t, dO) -
+                    _loss(QKV, Hq, Hkv, dh, ls - e, g, t, dO)) / (2 * eps)
+    fd_g = np.zeros(Hq)
+    for h in range(Hq):
+        e = np.zeros(Hq)
+        e[h] = eps
+        fd_g[h] = (_loss(QKV, Hq, Hkv, dh, ls, g + e, t, dO) -
+                   _loss(QKV, Hq, Hkv, dh, ls, g - e, t, dO)) / (2 * eps)
+    np.testing.assert_allclose(dls, fd_ls, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dgain, fd_g, rtol=1e-6, atol=1e-8)
+    # one head biased at a time: dL/dls then is that head's dL/db row
+    for h in range(Hq):
+        gh = np.zeros(Hq)
+        gh[h] = 1.0
+        dBh = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, gh, t, dO)
+        for j in (0, 7, M - 1):
+            e = np.zeros(M)
+            e[j] = eps
+            fd = (_loss(QKV, Hq, Hkv, dh, ls + e, gh, t, dO) -
+                  _loss(QKV, Hq, Hkv, dh, ls - e, gh, t, dO)) / (2 * eps)
+            assert abs(dBh[h, j] - fd) <= 1e-6 * max(1.0, abs(fd))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (2, 2), (6, 3)])
+def test_bias_grad_matches_sdpa_autograd(Hq, Hkv):
+    # torch's SDPA backward in float64 with a free [Hq][M] bias tensor: its
+    # gradient is dL/db; with g and ls as leaves it gives dL/dg and dL/dls
+    dh, M, t = 8, 29, 0.9
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=33 + Hq)
+    rng = np.random.default_rng(34)
+    ls = -rng.exponential(1.0, M)
+    g = rng.uniform(0.5, 1.5, Hq)
+    dO = rng.standard_normal((M, Hq * dh))
+    q, k, v = O.split_qkv(torch.from_numpy(QKV), Hq, Hkv, dh)
+    q = q.reshape(M, Hq, dh).transpose(0, 1)[None]
+    k = k.reshape(M, Hkv, dh).transpose(0, 1)[None]
+    v = v.reshape(M, Hkv, dh).transpose(0, 1)[None]
+    causal = torch.ones(M, M, dtype=torch.bool).tril()
+    gl = torch.tensor(g, requires_grad=True)
+    lsl = torch.tensor(ls, requires_grad=True)
+    bias = (gl[:, None] * lsl[None, :]).detach().requires_grad_(True)
+    outs = []
+    for b in (bias, gl[:, None] * lsl[None, :]):
+        mask = torch.where(causal[None], b[:, None, :].expand(Hq, M, M),
+                           torch.tensor(-math.inf, dtype=torch.float64))
+        out = F.scaled_dot_product_attention(q, k, v, attn_mask=mask[None],
+                                             scale=t / math.sqrt(dh), enable_gqa=True)
+        outs.append(out[0].transpose(0, 1).reshape(M, Hq * dh))
+    dOt = torch.from_numpy(dO)
+    (outs[0] * dOt).sum().backward()
+    (outs[1] * dOt).sum().backward()
+    dB = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO, chunk=10)
+    np.testing.assert_allclose(dB, bias.grad.numpy(), rtol=1e-10, atol=1e-12)
+    dls, dgain, _ = O.bias_grad_reduce(dB, ls, g)
+    np.testing.assert_allclose(dls, lsl.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dgain, gl.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_bias_grad_two_key_closed_form_and_shift_invariance():
+    # M = 2: row 0 sees only key 0 (P = 1, no gradient); row 1 mixes keys 0
+    # and 1 with weight sig = sigmoid(l_11 - l_10), so
+    #   dL/db_1 = sig (1 - sig) dO_1 . (v_1 - v_0) = -dL/db_0
+    Hq, Hkv, dh, t = 2, 1, 4, 1.3
+    QKV = _rand_qkv(2, Hq, Hkv, dh, seed=35)
+    ls = np.array([-0.4, -1.9])
+    g = np.array([0.8, 1.3])
+    dO = np.random.default_rng(36).standard_normal((2, Hq * dh))
+    dB = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO)
+    q, k, v = O.split_qkv(QKV, Hq, Hkv, dh)
+    for h in range(Hq):
+        qh = q[1, h * dh:(h + 1) * dh]
+        delta = t * (qh @ k[1] - qh @ k[0]) / math.sqrt(dh) + g[h] * (ls[1] - ls[0])
+        sig = 1.0 / (1.0 + math.exp(-delta))
+        want = sig * (1 - sig) * (dO[1, h * dh:(h + 1) * dh] @ (v[1] - v[0]))
+        assert abs(dB[h, 1] - want) < 1e-14
+        assert abs(dB[h, 0] + want) < 1e-14
+    # adding one constant to every key's bias changes no softmax row, so the
+    # bias gradient of each head sums to zero
+    Hq, Hkv, dh, M = 4, 2, 8, 40
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=37)
+    rng = np.random.default_rng(38)
+    dB = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, -rng.exponential(1.0, M),
+                                  rng.uniform(0.5, 1.5, Hq), 0.7, rng.standard_normal((M, Hq * dh)))
+    assert np.abs(dB.sum(axis=1)).max() < 1e-12 * np.abs(dB).max() * M
+    assert np.abs(dB).max() > 1e-3
+
+
+def test_bias_grad_of_the_score_through_logsigmoid():
+    # dL/ds by central differences through the pinned logsigmoid
+    Hq, Hkv, dh, M, t = 2, 1, 8, 12, 1.0
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=39)
+    rng = np.random.default_rng(40)
+    s = rng.standard_normal(M) * 3
+    s[0], s[1] = 40.0, -40.0            # the saturated ends of the sigmoid
+    g = rng.uniform(0.5, 1.5, Hq)
+    dO = rng.standard_normal((M, Hq * dh))
+    ls = O.logsigmoid(s)
+    _, _, ds = O.bias_grad_reduce(O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO), ls, g)
+    eps = 1e-6
+    for j in range(M):
+        e = np.zeros(M)
+        e[j] = eps
+        fd = (_loss(QKV, Hq, Hkv, dh, O.logsigmoid(s + e), g, t, dO) -
+              _loss(QKV, Hq, Hkv, dh, O.logsigmoid(s - e), g, t, dO)) / (2 * eps)
+        assert abs(ds[j] - fd) <= 1e-6 * abs(fd) + 1e-8, (j, ds[j], fd)   # FD rounding ~1e-9
+    # sigmoid(-40) ~ 4.2e-18 survives in -expm1(ls) (1 - exp(ls) would give 0)
+    assert ds[0] != 0.0 and abs(ds[0] / (O.bias_grad_reduce(
+        O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO), ls, g)[0][0]) -
+        1.0 / (1.0 + math.exp(40.0))) < 1e-25
+
+
+def test_lse_closed_forms_and_logsumexp():
+    Hq, Hkv, dh, M, t = 4, 2, 8, 33, 1.2
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=41)
+    g = np.array([0.5, 0.8, 1.1, 1.4])
+    # q = 0: every logit of row i is g_h c, so lse_i = g_h c + log(i + 1)
+    Z = QKV.copy()
+    Z[:, :Hq * dh] = 0.0
+    lse0 = O.keybias_attn_lse(Z, Hq, Hkv, dh, np.full(M, -0.6), g, t)
+    want = (g[:, None] * -0.6) + np.log(np.arange(1, M + 1))[None, :]
+    np.testing.assert_allclose(lse0, want, rtol=1e-14, atol=1e-14)
+    # general case: torch.logsumexp over the masked logit matrix
+    ls = -np.random.default_rng(42).exponential(1.0, M)
+    lse = O.keybias_attn_lse(QKV, Hq, Hkv, dh, ls, g, t, chunk=7)
+    q, k, _ = O.split_qkv(torch.from_numpy(QKV), Hq, Hkv, dh)
+    causal = torch.ones(M, M, dtype=torch.bool).tril()
+    for h in range(Hq):
+        hk = h // 2
+        logit = t * (q[:, h * dh:(h + 1) * dh] @ k[:, hk * dh:(hk + 1) * dh].T) / math.sqrt(dh)
+        logit = logit + g[h] * torch.from_numpy(ls)[None, :]
+        logit = torch.where(causal, logit, torch.tensor(-math.inf, dtype=torch.float64))
+        np.testing.assert_allclose(lse[h], torch.logsumexp(logit, dim=1).numpy(),
+                                   rtol=1e-13, atol=1e-13)
+    assert np.allclose(lse[:, 0], t * np.einsum("hd,hd->h",
+                       QKV[0, :Hq * dh].reshape(Hq, dh),
+                       np.repeat(QKV[0, Hq * dh:(Hq + Hkv) * dh].reshape(Hkv, dh), 2, axis=0))
+                       / math.sqrt(dh) + g * ls[0], rtol=1e-13, atol=1e-13)
+
+
+def test_attn_delta_brute_force_and_identity():
+    Hq, Hkv, dh, M = 3, 1, 5, 9
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=43)
+    rng = np.random.default_rng(44)
+    dO = rng.standard_normal((M, Hq * dh))
+    Oa = rng.standard_normal((M, Hq * dh))
+    D = O.attn_delta(dO, Oa, Hq, dh)
+    for h in range(Hq):
+        for i in range(M):
+            want = 0.0
+            for c in range(dh):
+                want += dO[i, h * dh + c] * Oa[i, h * dh + c]
+            assert abs(D[h, i] - want) < 1e-13
+    # with the exact attention output, dO_i . o_i = sum_j P_ij dP_ij, so the
+    # bias gradient computed from either form of D agrees: its row sums over
+    # keys vanish either way (checked above); here D itself is compared with
+    # sum_j P_ij dP_ij from the softmax written out by hand for row 2
+    ls = -rng.exponential(1.0, M)
+    g = np.array([0.6, 1.0, 1.4])
+    out = O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, 1.0)
+    D2 = O.attn_delta(dO, out, Hq, dh)
+    q, k, v = O.split_qkv(QKV, Hq, Hkv, dh)
+    for h in range(Hq):
+        i = 2
+        l = np.array([q[i, h * dh:(h + 1) * dh] @ k[j] / math.sqrt(dh) + g[h] * ls[j]
+                      for j in range(i + 1)])
+        p = np.exp(l - l.max())
+        p /= p.sum()
+        want = sum(p[j] * (dO[i, h * dh:(h + 1) * dh] @ v[j]) for j in range(i + 1))
+        assert abs(D2[h, i] - want) < 1e-13

@@ -31,12 +31,12 @@ import numpy as np
 __all__ = [
     "Workload", "WORKLOADS", "kept_count", "f32_to_bf16_bits",
     "residual", "gate_params", "qkv_weight", "attn_params", "rms_gamma",
-    "random_scores", "random_qkv", "random_logsig", "adversarial_scores",
+    "random_scores", "random_qkv", "random_logsig", "random_dout", "adversarial_scores",
 ]
 
 # stream ids: one per tensor kind, so that draws never overlap
 _S_RESIDUAL, _S_W1, _S_B1, _S_W2, _S_B2, _S_WQKV, _S_GAIN, _S_GAMMA = range(8)
-_S_SCORES, _S_QKV, _S_LOGSIG, _S_ADV = 20, 21, 22, 23
+_S_SCORES, _S_QKV, _S_LOGSIG, _S_ADV, _S_DOUT = 20, 21, 22, 23, 24
 
 
 @dataclass(frozen=True)
@@ -199,6 +199,12 @@ def random_qkv(M: int, Hq: int, Hkv: int, dh: int, seed: int, dtype: str = "bf16
                std: float = 1.0) -> np.ndarray:
     """Packed [M][(Hq + 2 Hkv) dh] q|k|v rows, for testing attention on its own."""
     return _normal(seed, _S_QKV, 0, (M, (Hq + 2 * Hkv) * dh), std, dtype)
+
+
+def random_dout(M: int, Hq: int, dh: int, seed: int, dtype: str = "bf16",
+                std: float = 1.0) -> np.ndarray:
+    """An upstream gradient dL/dO [M][Hq dh] for the attention output."""
+    return _normal(seed, _S_DOUT, 0, (M, Hq * dh), std, dtype)
 
 
 def random_logsig(M: int, seed: int) -> np.ndarray:
