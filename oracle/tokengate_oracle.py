@@ -314,9 +314,10 @@ def _head_logits(q, k, r, ls, g_h: float, t: float, dh: int) -> np.ndarray:
 
 
 def keybias_attn_lse(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain, temperature: float,
-                     chunk: int = 512) -> np.ndarray:
+                     chunk: int = 512, rows_from: int = 0) -> np.ndarray:
     """lse[h][i] = log sum_{j <= i} exp(l_ij), natural log, float64 [Hq][M]:
-    the per-row normaliser of the softmax that the backward re-uses."""
+    the per-row normaliser of the softmax that the backward re-uses.  Rows
+    below ``rows_from`` are left at 0 (not computed)."""
     Q = _widen(QKV)
     M = Q.shape[0]
     G = Hq // Hkv
@@ -328,7 +329,7 @@ def keybias_attn_lse(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain, tempera
         hk = h // G
         q = q_all[:, h * dh:(h + 1) * dh]
         k = k_all[:, hk * dh:(hk + 1) * dh]
-        for c0 in range(0, M, chunk):
+        for c0 in range(rows_from, M, chunk):
             r = np.arange(c0, min(M, c0 + chunk))
             logits = _head_logits(q, k, r, ls, g[h], float(temperature), dh)
             mx = logits.max(axis=1, keepdims=True)
@@ -346,11 +347,22 @@ def attn_delta(dO, O_out, Hq: int, dh: int) -> np.ndarray:
 
 
 def keybias_attn_bias_grad(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain,
-                           temperature: float, dO, chunk: int = 256) -> np.ndarray:
+                           temperature: float, dO, chunk: int = 256,
+                           return_terms: bool = False, keys_from: int = 0):
     """dL/db_hj = sum_{i >= j} P_ij (dP_ij - D_i) for every head h and kept
     key j, float64 [Hq][M], with P recomputed from the logits, dP_ij =
     dO_i . v_j and D_i = sum_j P_ij dP_ij (its definition, not dO_i . o_i).
-    ``logsig_kept`` None means b = 0 (the gradient is still defined)."""
+    ``logsig_kept`` None means b = 0 (the gradient is still defined).
+
+    With ``return_terms`` it also returns two magnitudes per (h, j) that size
+    the rounding of a finite-precision evaluation (they are not part of the
+    gradient): cond = sum_i P_ij (|dP_ij| + |D_i|), the sum of the absolute
+    terms, and oerr = sum_i P_ij sum_c |dO_ic| (|o_ic| + (P |V|)_ic), what a
+    relative error in every p and o element feeds into D and on into dL/db.
+
+    ``keys_from`` > 0 evaluates only the keys j >= keys_from: rows i <
+    keys_from (which reach no such key) are skipped, and the returned
+    columns below keys_from are 0."""
     Q = _widen(QKV)
     dOw = _widen(dO)
     M = Q.shape[0]
@@ -359,13 +371,15 @@ def keybias_attn_bias_grad(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain,
     ls = None if logsig_kept is None else np.asarray(logsig_kept, dtype=np.float64)
     g = np.asarray(gain, dtype=np.float64)
     dB = np.zeros((Hq, M), dtype=np.float64)
+    cond = np.zeros((Hq, M), dtype=np.float64)
+    oerr = np.zeros((Hq, M), dtype=np.float64)
     for h in range(Hq):
         hk = h // G
         q = q_all[:, h * dh:(h + 1) * dh]
         k = k_all[:, hk * dh:(hk + 1) * dh]
         v = v_all[:, hk * dh:(hk + 1) * dh]
         do = dOw[:, h * dh:(h + 1) * dh]
-        for c0 in range(0, M, chunk):
+        for c0 in range(keys_from, M, chunk):
             r = np.arange(c0, min(M, c0 + chunk))
             logits = _head_logits(q, k, r, ls, g[h], float(temperature), dh)
             jmax = logits.shape[1]
@@ -375,6 +389,17 @@ def keybias_attn_bias_grad(QKV, Hq: int, Hkv: int, dh: int, logsig_kept, gain,
             dp = do[r] @ v[:jmax].T
             D = (p * dp).sum(axis=1, keepdims=True)
             dB[h, :jmax] += (p * (dp - D)).sum(axis=0)
+            if return_terms:
+                cond[h, :jmax] += (p * (np.abs(dp) + np.abs(D))).sum(axis=0)
+                o = p @ v[:jmax]
+                w = (np.abs(do[r]) * (np.abs(o) + p @ np.abs(v[:jmax]))).sum(axis=1)
+                oerr[h, :jmax] += (p * w[:, None]).sum(axis=0)
+    if keys_from > 0:
+        dB[:, :keys_from] = 0.0
+        cond[:, :keys_from] = 0.0
+        oerr[:, :keys_from] = 0.0
+    if return_terms:
+        return dB, cond, oerr
     return dB
 
 

@@ -593,3 +593,51 @@ def test_attn_delta_brute_force_and_identity():
         p /= p.sum()
         want = sum(p[j] * (dO[i, h * dh:(h + 1) * dh] @ v[j]) for j in range(i + 1))
         assert abs(D2[h, i] - want) < 1e-13
+
+
+def test_bias_grad_terms_bound_a_perturbed_evaluation():
+    # the returned magnitudes bound what relative errors of size e in every
+    # p, dP and D (cond) and in every o fed to D (oerr) can do to dL/db
+    Hq, Hkv, dh, M, t = 2, 1, 16, 50, 1.0
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=45)
+    rng = np.random.default_rng(46)
+    ls = -rng.exponential(1.0, M)
+    g = np.array([0.7, 1.2])
+    dO = rng.standard_normal((M, Hq * dh))
+    dB, cond, oerr = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO, chunk=16,
+                                              return_terms=True)
+    assert np.array_equal(dB, O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO, chunk=16))
+    e = 1e-3
+    out = O.keybias_attn(QKV, Hq, Hkv, dh, ls, g, t)
+    o_pert = out * (1 + e * rng.choice([-1.0, 1.0], out.shape))
+    q, k, v = O.split_qkv(QKV, Hq, Hkv, dh)
+    for h in range(Hq):
+        l = t * (q[:, h * dh:(h + 1) * dh] @ k.T) / math.sqrt(dh) + g[h] * ls[None, :]
+        l = np.where(np.tril(np.ones((M, M), bool)), l, -np.inf)
+        p = np.exp(l - l.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        dp = dO[:, h * dh:(h + 1) * dh] @ v.T
+        D = (o_pert[:, h * dh:(h + 1) * dh] * dO[:, h * dh:(h + 1) * dh]).sum(axis=1)
+        got = (p * (dp - D[:, None])).sum(axis=0)
+        assert np.all(np.abs(got - dB[h]) <= e * oerr[h] * (1 + 1e-9) + 1e-12)
+        p2 = p * (1 + e * rng.choice([-1.0, 1.0], p.shape))
+        got2 = (p2 * (dp - (p * dp).sum(axis=1)[:, None])).sum(axis=0)
+        assert np.all(np.abs(got2 - dB[h]) <= e * cond[h] * (1 + 1e-9) + 1e-12)
+
+
+def test_bias_grad_and_lse_restricted_to_the_last_keys():
+    Hq, Hkv, dh, M, t = 4, 2, 8, 90, 1.1
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=47)
+    rng = np.random.default_rng(48)
+    ls = -rng.exponential(1.0, M)
+    g = rng.uniform(0.5, 1.5, Hq)
+    dO = rng.standard_normal((M, Hq * dh))
+    full = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO, return_terms=True)
+    part = O.keybias_attn_bias_grad(QKV, Hq, Hkv, dh, ls, g, t, dO, return_terms=True,
+                                    keys_from=61, chunk=7)
+    for a, b in zip(full, part):
+        np.testing.assert_allclose(b[:, 61:], a[:, 61:], rtol=1e-12, atol=1e-14)
+        assert not b[:, :61].any()
+    lse = O.keybias_attn_lse(QKV, Hq, Hkv, dh, ls, g, t)
+    lse_p = O.keybias_attn_lse(QKV, Hq, Hkv, dh, ls, g, t, rows_from=50, chunk=9)
+    np.testing.assert_allclose(lse_p[:, 50:], lse[:, 50:], rtol=1e-14, atol=1e-14)
