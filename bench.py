@@ -673,6 +673,142 @@ def run_compare(args, w, K, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------- the gradient path to the scorer
+BWD_KERNELS = ("attn_bwd_delta", "keybias_bias_grad", "bias_grad_reduce")
+
+
+def backward_work(w: TI.Workload, M: int) -> dict:
+    """Algorithmic bytes / flops of the three backward calls at M kept rows."""
+    Hq, dh, e = w.Hq, w.dh, 2
+    return {
+        "attn_bwd_delta": {"bytes": 2 * M * Hq * dh * e + Hq * M * 4, "flops": 0,
+                           "bound": "hbm"},
+        # S^T = K Q^T and dP^T = V dO^T over the causal half: 2 x 2 dh flops
+        # per (query, key) pair with key <= query, per q head
+        "keybias_bias_grad": {"bytes": M * w.qkv_cols * e + M * Hq * dh * e + 3 * Hq * M * 4
+                              + M * 4, "flops": 2 * M * M * dh * Hq, "bound": "tensor"},
+        "bias_grad_reduce": {"bytes": Hq * M * 4 + 3 * M * 4 + 2 * Hq * 4, "flops": 0,
+                             "bound": "hbm"},
+    }
+
+
+def run_backward(args, w, K, rank, world, local_rank):
+    """The gradient path from the attention output back to the scorer at the
+    workload's kept-row count M: D = dO . O, dL/db on the tensor cores, and
+    the reduction to dL/dlogsig, dL/dgain and dL/dscore.  Inputs are seeded
+    q|k|v, logsig, gain and an upstream gradient dO of the workload's shapes;
+    the forward (which writes O and lse) runs once, untimed.  Each timed step
+    is the three C-ABI calls with an event before and after each, and the L2
+    flushed between steps."""
+    import torch
+
+    import learned_token_pruning_residual_b300 as tg
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    L = tg.lib()
+    M = w.M(K)
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    qkv = to_dev(TI.random_qkv(M, w.Hq, w.Hkv, w.dh, seed=w.seed))
+    ls = to_dev(TI.random_logsig(M, seed=w.seed))
+    ap = TI.attn_params(w)
+    gain, t = to_dev(ap["gain"]), ap["temperature"]
+    dO = to_dev(TI.random_dout(M, w.Hq, w.dh, seed=w.seed))
+    out, lse = tg.tg_keybias_attn_lse(qkv, w.Hq, w.Hkv, w.dh, ls, gain, t)
+    f32 = torch.float32
+    delta = torch.empty(w.Hq, M, dtype=f32, device=dev)
+    dbias = torch.empty(w.Hq, M, dtype=f32, device=dev)
+    dls = torch.empty(M, dtype=f32, device=dev)
+    dgain = torch.empty(w.Hq, dtype=f32, device=dev)
+    dscore = torch.empty(M, dtype=f32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=f32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    P = {k: v.data_ptr() for k, v in dict(qkv=qkv, ls=ls, gain=gain, dO=dO, out=out, lse=lse,
+                                         delta=delta, dbias=dbias, dls=dls, dgain=dgain,
+                                         dscore=dscore).items()}
+
+    def check(st):
+        if st != 0:
+            raise tg.TokenGateError(st, L.tg_last_error_message().decode())
+
+    calls = [
+        lambda: check(L.tg_attn_bwd_delta(P["dO"], P["out"], 1, M, w.Hq, w.dh, P["delta"], sh)),
+        lambda: check(L.tg_keybias_attn_bias_grad(P["qkv"], P["dO"], 1, M, w.Hq, w.Hkv, w.dh,
+                                                  P["ls"], P["gain"], t, P["lse"], P["delta"],
+                                                  P["dbias"], sh)),
+        lambda: check(L.tg_bias_grad_reduce(P["dbias"], M, w.Hq, P["ls"], P["gain"], P["dls"],
+                                            P["dgain"], P["dscore"], sh)),
+    ]
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+           for _ in range(steps)]
+    for _ in range(warmup):
+        flush.zero_()
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    sampler.active = True
+    torch.cuda._sleep(50_000_000)
+    for k in range(steps):
+        flush.zero_()
+        evs[k][0].record(stream)
+        for i, c in enumerate(calls):
+            c()
+            evs[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.active = False
+    clocks = sampler.stop()
+    if tg.tg_get_device_status(raise_on_error=False) != 0:
+        raise RuntimeError("device status set during the backward")
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(len(calls))] for e in evs])
+    step_ms = float(np.mean([e[0].elapsed_time(e[-1]) for e in evs]))
+    work = backward_work(w, M)
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for i, name in enumerate(BWD_KERNELS):
+        ms = float(per[:, i].mean())
+        wk = work[name]
+        kernels[name] = {"ms": ms, "GB/s": wk["bytes"] / ms / 1e6,
+                         "TFLOP/s": wk["flops"] / ms / 1e9 if wk["flops"] else None}
+    wk, ms = work["keybias_bias_grad"], kernels["keybias_bias_grad"]["ms"]
+    ach = wk["flops"] / ms / 1e9
+    line = {
+        "metric": "token-gated attention backward to the scorer: prompt tokens/s",
+        "value": w.N / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "mode": "backward",
+        "config": {"workload": w.name, "N": w.N, "K": K, "M": M, "heads_q": w.Hq,
+                   "heads_kv": w.Hkv, "head_dim": w.dh,
+                   "l2": "flushed between steps (256 MiB write), outside the timed events",
+                   "launch": "direct C-ABI calls, an event before and after each"},
+        "roofline": {"kernel": "keybias_bias_grad", "bound": "tensor", "achieved": ach,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "algorithmic": wk["flops"], "peak_source": f"{peak_src} (bf16 burst)"},
+        "kernels": kernels,
+        "gpu_launches": len(calls) * steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
@@ -685,9 +821,10 @@ def main(argv=None) -> int:
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the five calls directly instead of replaying one CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="step", choices=["step", "compare"],
+    ap.add_argument("--mode", default="step", choices=["step", "compare", "backward"],
                     help="step: the timed gated-prefill step (default); compare: gated path vs "
-                         "full prefill on the same kernels, with peak device memory")
+                         "full prefill on the same kernels, with peak device memory; backward: "
+                         "the gradient path from the attention bias to the scorer")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     w = TI.WORKLOADS[args.workload]
@@ -696,6 +833,8 @@ def main(argv=None) -> int:
         return run_reference(args, w, K, rank, world)
     if args.mode == "compare":
         return run_compare(args, w, K, rank, world, local_rank)
+    if args.mode == "backward":
+        return run_backward(args, w, K, rank, world, local_rank)
     return run_gpu(args, w, K, rank, world, local_rank)
 
 

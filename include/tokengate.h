@@ -66,7 +66,7 @@ typedef enum tg_dtype { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
 const char* tg_status_string(int status);
 
 /* ABI version of this header (bumped on any signature change). */
-#define TG_ABI_VERSION 1
+#define TG_ABI_VERSION 2
 int tg_abi_version(void);
 
 /* Message of the last TG_ERR_INVALID_ARG / TG_ERR_UNSUPPORTED / TG_ERR_CUDA
@@ -194,6 +194,74 @@ tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M,
                           const float* logsig_kept, const float* gain,
                           float temperature, void* O, float* residual,
                           tg_stream_t stream);
+
+/*
+ * tg_keybias_attn, and also the per-row normaliser that a backward pass
+ * re-uses:  lse[h][i] = log sum_{j <= i} exp(l_ij)  (natural log), fp32,
+ * [Hq][M] densely packed (row h starts at lse + h * M).  Same arguments and
+ * limits as tg_keybias_attn; lse must not be NULL when M > 0.
+ */
+tg_status tg_keybias_attn_lse(const void* QKV, tg_dtype dtype, int64_t M,
+                              int32_t Hq, int32_t Hkv, int32_t dh,
+                              const float* logsig_kept, const float* gain,
+                              float temperature, void* O, float* residual,
+                              float* lse, tg_stream_t stream);
+
+/*
+ * ---- The gradient the bias carries back to the scorer ([DE] "Was ist
+ * token-gated Attention?": the kept token's score becomes a bias on the
+ * attention logits, which gives the gradient a path back to the scorer;
+ * [TH] the same, MoE-router style).  With b_hj = g_h * logsig_kept[j] and an
+ * upstream gradient dO = dL/dO of the attention output, the chain rule gives
+ *   dL/db_hj = sum_{i >= j} P_ij (dO_i . v_j - D_i),  D_i = dO_i . o_i,
+ * with P_ij = exp(l_ij - lse_i) and dO_i, o_i the dh columns of head h.
+ * The four calls, in order: tg_keybias_attn_lse (forward), tg_attn_bwd_delta,
+ * tg_keybias_attn_bias_grad, tg_bias_grad_reduce.
+ */
+
+/*
+ * D[h][i] = sum_c dO[i][h dh + c] * O[i][h dh + c], accumulated in fp32.
+ *  dO, O   [M][Hq dh] in `dtype` (O as written by the forward).
+ *  delta   [Hq][M] fp32 output, densely packed.
+ * Limits: TG_BF16: dh in {64, 128, 256}; TG_F32: dh in {32, 64, 128}.
+ */
+tg_status tg_attn_bwd_delta(const void* dO, const void* O, tg_dtype dtype,
+                            int64_t M, int32_t Hq, int32_t dh, float* delta,
+                            tg_stream_t stream);
+
+/*
+ * dbias[h][j] = dL/db_hj for every q head h and kept row j (fp32, [Hq][M]
+ * densely packed): P is recomputed from QKV, logsig_kept, gain, temperature
+ * and lse (as tg_keybias_attn_lse wrote it), and D comes from
+ * tg_attn_bwd_delta.  TG_BF16: tcgen05 tensor cores, fp32 accumulation;
+ * TG_F32: CUDA cores.
+ *  QKV          [M][(Hq + 2 Hkv) dh] in `dtype`; dO [M][Hq dh] in `dtype`.
+ *  logsig_kept  [M] fp32 or NULL (no bias: b = 0); gain [Hq] fp32.
+ *  lse, delta   [Hq][M] fp32.
+ * Limits: Hq % Hkv == 0; t finite; TG_BF16: dh == 128; TG_F32: dh in
+ * {32, 64, 128}.
+ */
+tg_status tg_keybias_attn_bias_grad(const void* QKV, const void* dO,
+                                    tg_dtype dtype, int64_t M, int32_t Hq,
+                                    int32_t Hkv, int32_t dh,
+                                    const float* logsig_kept,
+                                    const float* gain, float temperature,
+                                    const float* lse, const float* delta,
+                                    float* dbias, tg_stream_t stream);
+
+/*
+ * From dbias [Hq][M] (all fp32):
+ *   dlogsig[j] = sum_h gain[h] * dbias[h][j]            (dL/d logsig_kept)
+ *   dgain[h]   = sum_j logsig_kept[j] * dbias[h][j]     (dL/dg)
+ *   dscore[j]  = dlogsig[j] * sigmoid(-s_j)              (dL/ds of kept token j,
+ *                with sigmoid(-s) = -expm1(logsig_kept[j]); NULL to skip)
+ * Pruned tokens get no gradient through this path.  Fixed summation order:
+ * the results are bitwise reproducible.  M == 0 writes dgain = 0.
+ */
+tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
+                              const float* logsig_kept, const float* gain,
+                              float* dlogsig, float* dgain, float* dscore,
+                              tg_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the sticky device status

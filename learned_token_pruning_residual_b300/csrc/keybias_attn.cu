@@ -55,6 +55,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = kBK * kDH * 2;  // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // The key bias rides in one extra K = 16 block of the Q K^T product: 128 rows
 // x 16 bf16, K-major without swizzle (8-row x 16-byte core matrices, 128 B
@@ -74,6 +75,7 @@ struct AttnArgs {
   const float* gain;
   __nv_bfloat16* O;
   float* residual;
+  float* lse;   // [Hq][M] natural-log row normalisers, or null
   int64_t ldo;  // Hq * dh
   uint32_t* status;
 };
@@ -252,6 +254,9 @@ __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& ar
   if (!have) return;
   const bool row_ok = row < args.M;
   const float inv = 1.f / l_run;
+  // log sum_j exp(l_ij) = (m_run + log2 l_run) ln 2, for a backward pass
+  if (args.lse != nullptr && row_ok)
+    args.lse[static_cast<int64_t>(h) * args.M + row] = (m_run + log2f(l_run)) * kLn2;
 #pragma unroll 1
   for (int c0 = 0; c0 < kDH; c0 += 32) {
     uint32_t w[32];
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
                              const float* logsig, const float* gain, float temperature, void* O,
-                             float* residual, cudaStream_t stream) {
+                             float* residual, float* lse, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
   AttnArgs a{};
   a.M = static_cast<int>(M);
@@ -548,6 +553,7 @@ cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh
   a.gain = gain;
   a.O = static_cast<__nv_bfloat16*>(O);
   a.residual = residual;
+  a.lse = lse;
   a.ldo = static_cast<int64_t>(Hq) * dh;
   a.status = device_status_word();
   const int cols = (Hq + 2 * Hkv) * dh;

@@ -97,7 +97,7 @@ template <int DH>
 __global__ void __launch_bounds__(64)
     attn_f32_kernel(const float* __restrict__ QKV, int64_t M, int Hq, int Hkv,
                     const float* __restrict__ ls, const float* __restrict__ gain, float scale,
-                    float* __restrict__ O, float* __restrict__ residual) {
+                    float* __restrict__ O, float* __restrict__ residual, float* __restrict__ lse) {
   constexpr int kKeys = DH == 128 ? 32 : 64;  // 32 KB of keys and values at most
   __shared__ float ks[kKeys][DH];
   __shared__ float vs[kKeys][DH];
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(64)
     }
   }
   if (!valid) return;
+  if (lse != nullptr) lse[static_cast<int64_t>(h) * M + i] = m + logf(l);
   const float inv = 1.f / l;
   const int64_t ldo = static_cast<int64_t>(Hq) * DH;
 #pragma unroll
@@ -190,19 +191,19 @@ cudaError_t launch_qkv_f32(const float* X, int64_t M, int d, const float* W, int
 
 cudaError_t launch_attn_f32(const float* QKV, int64_t M, int Hq, int Hkv, int dh,
                             const float* logsig, const float* gain, float temperature, float* O,
-                            float* residual, cudaStream_t stream) {
+                            float* residual, float* lse, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((M + 63) / 64), Hq);
   const float scale = temperature / sqrtf(static_cast<float>(dh));
   switch (dh) {
     case 32:
-      attn_f32_kernel<32><<<grid, 64, 0, stream>>>(QKV, M, Hq, Hkv, logsig, gain, scale, O, residual);
+      attn_f32_kernel<32><<<grid, 64, 0, stream>>>(QKV, M, Hq, Hkv, logsig, gain, scale, O, residual, lse);
       break;
     case 64:
-      attn_f32_kernel<64><<<grid, 64, 0, stream>>>(QKV, M, Hq, Hkv, logsig, gain, scale, O, residual);
+      attn_f32_kernel<64><<<grid, 64, 0, stream>>>(QKV, M, Hq, Hkv, logsig, gain, scale, O, residual, lse);
       break;
     case 128:
-      attn_f32_kernel<128><<<grid, 64, 0, stream>>>(QKV, M, Hq, Hkv, logsig, gain, scale, O, residual);
+      attn_f32_kernel<128><<<grid, 64, 0, stream>>>(QKV, M, Hq, Hkv, logsig, gain, scale, O, residual, lse);
       break;
     default:
       return cudaErrorInvalidValue;

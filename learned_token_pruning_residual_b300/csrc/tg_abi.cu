@@ -123,6 +123,40 @@ tg_status from_cuda(cudaError_t e, const char* what) {
     if (!(cond)) return fail(code, __VA_ARGS__); \
   } while (0)
 
+// Token-gated attention, optionally writing the per-row log-sum-exp.
+tg_status keybias_attn_impl(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq, int32_t Hkv,
+                            int32_t dh, const float* logsig_kept, const float* gain,
+                            float temperature, void* O, float* residual, float* lse,
+                            tg_stream_t stream) {
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "attn: bad dtype");
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && Hkv > 0 && dh > 0,
+             TG_ERR_INVALID_ARG, "attn: bad sizes");
+  TG_REQUIRE(Hq % Hkv == 0, TG_ERR_INVALID_ARG, "attn: Hq %% Hkv != 0");
+  TG_REQUIRE(temperature == temperature, TG_ERR_INVALID_ARG, "attn: temperature is NaN");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(QKV && (O || residual), TG_ERR_INVALID_ARG, "attn: NULL pointer");
+  TG_REQUIRE(!logsig_kept || gain, TG_ERR_INVALID_ARG, "attn: gain needed with a bias");
+  TG_REQUIRE(aligned16(QKV) && (!O || aligned16(O)) && (!residual || aligned16(residual)) &&
+                 (!logsig_kept || aligned16(logsig_kept)) && (!lse || aligned16(lse)),
+             TG_ERR_INVALID_ARG, "attn: pointers must be 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TG_BF16) {
+    TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "attn bf16: dh must be 128");
+    TG_REQUIRE((Hq / Hkv) % 2 == 0, TG_ERR_UNSUPPORTED, "attn bf16: Hq / Hkv must be even");
+    TG_REQUIRE(temperature > 0.f && temperature <= 3.0e38f, TG_ERR_UNSUPPORTED,
+               "attn bf16: temperature must be finite and > 0");
+    return from_cuda(tg::launch_attn_bf16(QKV, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
+                                          residual, lse, st),
+                     "attn bf16");
+  }
+  TG_REQUIRE(dh == 32 || dh == 64 || dh == 128, TG_ERR_UNSUPPORTED,
+             "attn f32: dh must be 32, 64 or 128");
+  return from_cuda(tg::launch_attn_f32(static_cast<const float*>(QKV), M, Hq, Hkv, dh,
+                                       logsig_kept, gain, temperature, static_cast<float*>(O),
+                                       residual, lse, st),
+                   "attn f32");
+}
+
 }  // namespace
 
 extern "C" {
@@ -253,33 +287,83 @@ tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d, const
 tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq, int32_t Hkv,
                           int32_t dh, const float* logsig_kept, const float* gain,
                           float temperature, void* O, float* residual, tg_stream_t stream) {
-  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "attn: bad dtype");
-  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && Hkv > 0 && dh > 0,
-             TG_ERR_INVALID_ARG, "attn: bad sizes");
-  TG_REQUIRE(Hq % Hkv == 0, TG_ERR_INVALID_ARG, "attn: Hq %% Hkv != 0");
-  TG_REQUIRE(temperature == temperature, TG_ERR_INVALID_ARG, "attn: temperature is NaN");
+  return keybias_attn_impl(QKV, dtype, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
+                           residual, nullptr, stream);
+}
+
+tg_status tg_keybias_attn_lse(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq,
+                              int32_t Hkv, int32_t dh, const float* logsig_kept,
+                              const float* gain, float temperature, void* O, float* residual,
+                              float* lse, tg_stream_t stream) {
+  TG_REQUIRE(lse || M == 0, TG_ERR_INVALID_ARG, "attn lse: NULL lse");
+  return keybias_attn_impl(QKV, dtype, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
+                           residual, lse, stream);
+}
+
+tg_status tg_attn_bwd_delta(const void* dO, const void* O, tg_dtype dtype, int64_t M, int32_t Hq,
+                            int32_t dh, float* delta, tg_stream_t stream) {
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "delta: bad dtype");
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && dh > 0, TG_ERR_INVALID_ARG,
+             "delta: bad sizes");
+  TG_REQUIRE(dtype == TG_BF16 ? (dh == 64 || dh == 128 || dh == 256)
+                              : (dh == 32 || dh == 64 || dh == 128),
+             TG_ERR_UNSUPPORTED, "delta: dh must be 64, 128 or 256 (bf16), 32, 64 or 128 (f32)");
   if (M == 0) return TG_OK;
-  TG_REQUIRE(QKV && (O || residual), TG_ERR_INVALID_ARG, "attn: NULL pointer");
-  TG_REQUIRE(!logsig_kept || gain, TG_ERR_INVALID_ARG, "attn: gain needed with a bias");
-  TG_REQUIRE(aligned16(QKV) && (!O || aligned16(O)) && (!residual || aligned16(residual)) &&
-                 (!logsig_kept || aligned16(logsig_kept)),
-             TG_ERR_INVALID_ARG, "attn: pointers must be 16-byte aligned");
+  TG_REQUIRE(dO && O && delta, TG_ERR_INVALID_ARG, "delta: NULL pointer");
+  TG_REQUIRE(aligned16(dO) && aligned16(O) && aligned16(delta), TG_ERR_INVALID_ARG,
+             "delta: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_attn_delta(dO, O, dtype == TG_BF16, M, Hq, dh, delta,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                   "delta");
+}
+
+tg_status tg_keybias_attn_bias_grad(const void* QKV, const void* dO, tg_dtype dtype, int64_t M,
+                                    int32_t Hq, int32_t Hkv, int32_t dh,
+                                    const float* logsig_kept, const float* gain,
+                                    float temperature, const float* lse, const float* delta,
+                                    float* dbias, tg_stream_t stream) {
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "bias grad: bad dtype");
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && Hkv > 0 && dh > 0,
+             TG_ERR_INVALID_ARG, "bias grad: bad sizes");
+  TG_REQUIRE(Hq % Hkv == 0, TG_ERR_INVALID_ARG, "bias grad: Hq %% Hkv != 0");
+  TG_REQUIRE(temperature == temperature && temperature <= 3.0e38f && temperature >= -3.0e38f,
+             TG_ERR_INVALID_ARG, "bias grad: temperature must be finite");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(QKV && dO && lse && delta && dbias, TG_ERR_INVALID_ARG, "bias grad: NULL pointer");
+  TG_REQUIRE(!logsig_kept || gain, TG_ERR_INVALID_ARG, "bias grad: gain needed with a bias");
+  TG_REQUIRE(aligned16(QKV) && aligned16(dO) && aligned16(lse) && aligned16(delta) &&
+                 aligned16(dbias) && (!logsig_kept || aligned16(logsig_kept)),
+             TG_ERR_INVALID_ARG, "bias grad: pointers must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TG_BF16) {
-    TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "attn bf16: dh must be 128");
-    TG_REQUIRE((Hq / Hkv) % 2 == 0, TG_ERR_UNSUPPORTED, "attn bf16: Hq / Hkv must be even");
-    TG_REQUIRE(temperature > 0.f && temperature <= 3.0e38f, TG_ERR_UNSUPPORTED,
-               "attn bf16: temperature must be finite and > 0");
-    return from_cuda(tg::launch_attn_bf16(QKV, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
-                                          residual, st),
-                     "attn bf16");
+    TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "bias grad bf16: dh must be 128");
+    return from_cuda(tg::launch_bias_grad_bf16(QKV, dO, M, Hq, Hkv, dh, logsig_kept, gain,
+                                               temperature, lse, delta, dbias, st),
+                     "bias grad bf16");
   }
   TG_REQUIRE(dh == 32 || dh == 64 || dh == 128, TG_ERR_UNSUPPORTED,
-             "attn f32: dh must be 32, 64 or 128");
-  return from_cuda(tg::launch_attn_f32(static_cast<const float*>(QKV), M, Hq, Hkv, dh,
-                                       logsig_kept, gain, temperature, static_cast<float*>(O),
-                                       residual, st),
-                   "attn f32");
+             "bias grad f32: dh must be 32, 64 or 128");
+  return from_cuda(tg::launch_bias_grad_f32(static_cast<const float*>(QKV),
+                                            static_cast<const float*>(dO), M, Hq, Hkv, dh,
+                                            logsig_kept, gain, temperature, lse, delta, dbias,
+                                            st),
+                   "bias grad f32");
+}
+
+tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
+                              const float* logsig_kept, const float* gain, float* dlogsig,
+                              float* dgain, float* dscore, tg_stream_t stream) {
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0, TG_ERR_INVALID_ARG,
+             "bias grad reduce: bad sizes");
+  TG_REQUIRE(dgain && gain, TG_ERR_INVALID_ARG, "bias grad reduce: NULL pointer");
+  TG_REQUIRE(M == 0 || (dbias && logsig_kept && dlogsig), TG_ERR_INVALID_ARG,
+             "bias grad reduce: NULL pointer");
+  TG_REQUIRE(aligned16(dgain) && aligned16(gain) && (M == 0 || (aligned16(dbias) &&
+             aligned16(logsig_kept) && aligned16(dlogsig))) && (!dscore || aligned16(dscore)),
+             TG_ERR_INVALID_ARG, "bias grad reduce: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_bias_grad_reduce(dbias, M, Hq, logsig_kept, gain, dlogsig, dgain,
+                                               dscore, reinterpret_cast<cudaStream_t>(stream)),
+                   "bias grad reduce");
 }
 
 tg_status tg_get_device_status(tg_stream_t stream) {

@@ -79,9 +79,22 @@ cudaError_t launch_rmsnorm(const void* X, int x_bf16, int64_t M, int d, const fl
                            float eps, void* Y, int y_bf16, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
                              const float* logsig, const float* gain, float temperature, void* O,
-                             float* residual, cudaStream_t stream);
+                             float* residual, float* lse, cudaStream_t stream);
 cudaError_t launch_attn_f32(const float* QKV, int64_t M, int Hq, int Hkv, int dh,
                             const float* logsig, const float* gain, float temperature, float* O,
-                            float* residual, cudaStream_t stream);
+                            float* residual, float* lse, cudaStream_t stream);
+cudaError_t launch_attn_delta(const void* dO, const void* O, int x_bf16, int64_t M, int Hq,
+                              int dh, float* delta, cudaStream_t stream);
+cudaError_t launch_bias_grad_bf16(const void* QKV, const void* dO, int64_t M, int Hq, int Hkv,
+                                  int dh, const float* ls, const float* gain, float temperature,
+                                  const float* lse, const float* delta, float* dbias,
+                                  cudaStream_t stream);
+cudaError_t launch_bias_grad_f32(const float* QKV, const float* dO, int64_t M, int Hq, int Hkv,
+                                 int dh, const float* ls, const float* gain, float temperature,
+                                 const float* lse, const float* delta, float* dbias,
+                                 cudaStream_t stream);
+cudaError_t launch_bias_grad_reduce(const float* dbias, int64_t M, int Hq, const float* ls,
+                                    const float* gain, float* dls, float* dgain, float* dscore,
+                                    cudaStream_t stream);
 
 }  // namespace tg

@@ -13,9 +13,14 @@ Functions carry the C names:
     tg_rmsnorm        RMSNorm of a pruned layer's input
     tg_qkv_proj       packed q|k|v projection of the kept rows
     tg_keybias_attn   causal GQA attention with the per-key bias g_h * logsig
+    tg_keybias_attn_lse        the same, also writing each row's log-sum-exp
+    tg_attn_bwd_delta          D = dO . O per head and row
+    tg_keybias_attn_bias_grad  dL/db for the per-head key bias b = g_h * logsig
+    tg_bias_grad_reduce        dL/dlogsig, dL/dgain and dL/dscore from dL/db
     tg_get_device_status
 
-plus two compositions of them, ``gated_layer`` and ``pruned_stack``.
+plus three compositions of them, ``gated_layer``, ``pruned_stack`` and
+``bias_backward``.
 """
 from __future__ import annotations
 
@@ -27,8 +32,9 @@ import torch
 __all__ = [
     "TokenGateError", "lib", "library_path", "TG_F32", "TG_BF16",
     "tg_gate_score", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
-    "tg_keybias_attn", "tg_get_device_status", "gated_layer", "pruned_stack",
-    "EXPORTED_SYMBOLS",
+    "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
+    "tg_bias_grad_reduce", "tg_get_device_status", "gated_layer", "pruned_stack",
+    "bias_backward", "EXPORTED_SYMBOLS",
 ]
 
 TG_F32, TG_BF16 = 0, 1
@@ -50,6 +56,12 @@ _SIGNATURES = {
     "tg_rmsnorm": [_p, ctypes.c_int, _i64, _i32, _p, _f32, _p, ctypes.c_int, _p],
     "tg_qkv_proj": [_p, ctypes.c_int, _i64, _i32, _p, _i32, _i32, _i32, _p, _p],
     "tg_keybias_attn": [_p, ctypes.c_int, _i64, _i32, _i32, _i32, _p, _p, _f32, _p, _p, _p],
+    "tg_keybias_attn_lse": [_p, ctypes.c_int, _i64, _i32, _i32, _i32, _p, _p, _f32, _p, _p, _p,
+                            _p],
+    "tg_attn_bwd_delta": [_p, _p, ctypes.c_int, _i64, _i32, _i32, _p, _p],
+    "tg_keybias_attn_bias_grad": [_p, _p, ctypes.c_int, _i64, _i32, _i32, _i32, _p, _p, _f32, _p,
+                                  _p, _p, _p],
+    "tg_bias_grad_reduce": [_p, _i64, _i32, _p, _p, _p, _p, _p, _p],
     "tg_get_device_status": [_p],
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -179,6 +191,58 @@ def tg_keybias_attn(QKV, Hq: int, Hkv: int, dh: int, logsig, gain, temperature: 
     return out if residual is None else residual
 
 
+def tg_keybias_attn_lse(QKV, Hq: int, Hkv: int, dh: int, logsig, gain, temperature: float,
+                        out=None, residual=None, lse=None):
+    """(O, lse): tg_keybias_attn plus lse [Hq][M] fp32, the natural-log
+    normaliser log sum_{j <= i} exp(l_ij) of every head and row."""
+    M = QKV.shape[0]
+    if out is None and residual is None:
+        out = torch.empty(M, Hq * dh, dtype=QKV.dtype, device=QKV.device)
+    if lse is None:
+        lse = torch.empty(Hq, M, dtype=torch.float32, device=QKV.device)
+    _check(lib().tg_keybias_attn_lse(_ptr(QKV), _dt(QKV), M, Hq, Hkv, dh, _ptr(logsig),
+                                     _ptr(gain), float(temperature), _ptr(out), _ptr(residual),
+                                     _ptr(lse), _stream()))
+    return (out if residual is None else residual), lse
+
+
+def tg_attn_bwd_delta(dO, O, Hq: int, dh: int, out=None):
+    """D [Hq][M] fp32: dO_i . o_i over the dh columns of each head."""
+    M = dO.shape[0]
+    if out is None:
+        out = torch.empty(Hq, M, dtype=torch.float32, device=dO.device)
+    _check(lib().tg_attn_bwd_delta(_ptr(dO), _ptr(O), _dt(dO), M, Hq, dh, _ptr(out), _stream()))
+    return out
+
+
+def tg_keybias_attn_bias_grad(QKV, dO, Hq: int, Hkv: int, dh: int, logsig, gain,
+                              temperature: float, lse, delta, out=None):
+    """dL/db [Hq][M] fp32 for the key bias b_hj = g_h logsig_j."""
+    M = QKV.shape[0]
+    if out is None:
+        out = torch.empty(Hq, M, dtype=torch.float32, device=QKV.device)
+    _check(lib().tg_keybias_attn_bias_grad(_ptr(QKV), _ptr(dO), _dt(QKV), M, Hq, Hkv, dh,
+                                           _ptr(logsig), _ptr(gain), float(temperature),
+                                           _ptr(lse), _ptr(delta), _ptr(out), _stream()))
+    return out
+
+
+def tg_bias_grad_reduce(dbias, logsig, gain, dlogsig=None, dgain=None, dscore=None,
+                        want_dscore: bool = True):
+    """(dL/dlogsig [M], dL/dgain [Hq], dL/dscore [M] or None) from dL/db."""
+    Hq, M = dbias.shape
+    dev = dbias.device
+    if dlogsig is None:
+        dlogsig = torch.empty(M, dtype=torch.float32, device=dev)
+    if dgain is None:
+        dgain = torch.empty(Hq, dtype=torch.float32, device=dev)
+    if dscore is None and want_dscore:
+        dscore = torch.empty(M, dtype=torch.float32, device=dev)
+    _check(lib().tg_bias_grad_reduce(_ptr(dbias), M, Hq, _ptr(logsig), _ptr(gain), _ptr(dlogsig),
+                                     _ptr(dgain), _ptr(dscore), _stream()))
+    return dlogsig, dgain, dscore
+
+
 def tg_get_device_status(raise_on_error: bool = True) -> int:
     st = lib().tg_get_device_status(_stream())
     if raise_on_error:
@@ -214,3 +278,18 @@ def pruned_stack(x, layers, Hq, Hkv, dh, logsig, eps: float = 1e-6, bufs: dict |
         tg_qkv_proj(xn, L["Wqkv"], Hq, Hkv, dh, out=qkv)
         tg_keybias_attn(qkv, Hq, Hkv, dh, logsig, L["gain"], L["temperature"], residual=x)
     return x
+
+
+def bias_backward(qkv, O, lse, dO, Hq, Hkv, dh, logsig, gain, temperature,
+                  bufs: dict | None = None):
+    """The gradient path from the attention output back to the scorer, three
+    library calls on the current stream: D = dO . O, dL/db, then dL/dlogsig,
+    dL/dgain and dL/dscore.  ``O`` and ``lse`` come from tg_keybias_attn_lse.
+    ``bufs`` may hold preallocated outputs (delta, dbias, dlogsig, dgain, dscore)."""
+    b = bufs or {}
+    delta = tg_attn_bwd_delta(dO, O, Hq, dh, out=b.get("delta"))
+    dbias = tg_keybias_attn_bias_grad(qkv, dO, Hq, Hkv, dh, logsig, gain, temperature, lse, delta,
+                                      out=b.get("dbias"))
+    dls, dg, ds = tg_bias_grad_reduce(dbias, logsig, gain, dlogsig=b.get("dlogsig"),
+                                      dgain=b.get("dgain"), dscore=b.get("dscore"))
+    return {"delta": delta, "dbias": dbias, "dlogsig": dls, "dgain": dg, "dscore": ds}

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.tg_abi_version() == 1
+    assert L.tg_abi_version() == 2
     names = [L.tg_status_string(i).decode() for i in range(7)]
     assert names == ["TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
                      "TG_ERR_NAN_SCORE", "TG_ERR_BAD_INDEX", "TG_ERR_TIMEOUT"]
@@ -114,3 +114,41 @@ def test_python_binding_raises_without_device():
     x = torch.zeros(4, 64)
     with pytest.raises(ValueError):
         tg.tg_gate_score(x, x, None, x[0], 0.0)
+
+
+def test_backward_argument_errors(L):
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    # forward with lse: a NULL lse is an error, M == 0 launches nothing
+    assert L.tg_keybias_attn_lse(p, 1, 10, 16, 8, 128, None, None, 1.0, p, None, None, None) == 1
+    assert L.tg_keybias_attn_lse(None, 1, 0, 16, 8, 128, None, None, 1.0, None, None, None,
+                                 None) == 0
+    assert L.tg_keybias_attn_lse(p, 1, 10, 16, 8, 128, None, None, 1.0, p, None, odd, None) == 1
+    # delta: dtype, sizes, unsupported dh, NULL and misaligned pointers
+    assert L.tg_attn_bwd_delta(p, p, 7, 10, 16, 128, p, None) == 1
+    assert L.tg_attn_bwd_delta(p, p, 1, -1, 16, 128, p, None) == 1
+    assert L.tg_attn_bwd_delta(p, p, 1, 10, 16, 96, p, None) == 2
+    assert L.tg_attn_bwd_delta(p, p, 0, 10, 16, 256, p, None) == 2
+    assert L.tg_attn_bwd_delta(p, None, 1, 10, 16, 128, p, None) == 1
+    assert L.tg_attn_bwd_delta(p, odd, 1, 10, 16, 128, p, None) == 1
+    assert L.tg_attn_bwd_delta(None, None, 1, 0, 16, 128, None, None) == 0
+    # bias gradient
+    args = lambda **kw: [kw.get("qkv", p), kw.get("do", p), kw.get("dt", 1), kw.get("M", 10),
+                         kw.get("Hq", 16), kw.get("Hkv", 8), kw.get("dh", 128), kw.get("ls", p),
+                         kw.get("g", p), kw.get("t", 1.0), kw.get("lse", p), kw.get("delta", p),
+                         kw.get("db", p), None]
+    assert L.tg_keybias_attn_bias_grad(*args(dt=5)) == 1
+    assert L.tg_keybias_attn_bias_grad(*args(Hq=12)) == 1                 # Hq % Hkv
+    assert L.tg_keybias_attn_bias_grad(*args(t=float("nan"))) == 1
+    assert L.tg_keybias_attn_bias_grad(*args(t=float("inf"))) == 1
+    assert L.tg_keybias_attn_bias_grad(*args(lse=None)) == 1
+    assert L.tg_keybias_attn_bias_grad(*args(g=None)) == 1                # bias without gain
+    assert L.tg_keybias_attn_bias_grad(*args(db=odd)) == 1
+    assert L.tg_keybias_attn_bias_grad(*args(dh=64)) == 2                 # bf16 needs dh 128
+    assert L.tg_keybias_attn_bias_grad(*args(dt=0, dh=96)) == 2
+    assert L.tg_keybias_attn_bias_grad(*args(M=0, qkv=None, do=None)) == 0
+    # reduction
+    assert L.tg_bias_grad_reduce(p, 10, 0, p, p, p, p, None, None) == 1     # Hq
+    assert L.tg_bias_grad_reduce(p, 10, 4, None, p, p, p, None, None) == 1  # logsig
+    assert L.tg_bias_grad_reduce(p, 10, 4, p, p, p, None, None, None) == 1  # dgain
+    assert L.tg_bias_grad_reduce(p, 10, 4, p, p, p, p, odd, None) == 1      # dscore alignment
