@@ -42,14 +42,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 KERNELS = ("gate_score", "select_topk", "gather_rows", "qkv_proj", "keybias_attn")
 KERNEL_SOURCES = {"gate_score": "gemm_tc.cu", "select_topk": "select_topk.cu",
                   "gather_rows": "rows.cu", "qkv_proj": "gemm_tc.cu",
-                  "keybias_attn": "keybias_attn.cu"}
+                  "keybias_attn": "keybias_attn.cu", "keybias_bias_grad": "attn_bwd.cu"}
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by workload/kernel, with the sha256 (first 16
 # hex) of the kernel's source at capture time; a stale hash reports null.
 NCU_TRAFFIC: dict[str, dict] = {
     # Qwen3-1.7B shapes, N = 16384, 10% kept (profiles/*_qwen3_n16k.md)
-    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15378432 + 2048,
-                                            "source_sha": "3b72f3aa1585c90c"},
+    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15383552 + 768,
+                                            "source_sha": "9cd3022e6e5e9867"},
     "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68187904 + 627456,
                                           "source_sha": "25e1c47fd2f58bc2"},
     "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24447744 + 512,
@@ -59,12 +59,15 @@ NCU_TRAFFIC: dict[str, dict] = {
     "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 92672,
                                            "source_sha": "eab745ed225e14e2"},
     # N = 131072, 6.25% kept (profiles/keybias_attn_qwen3_n128k.md, gemm_gate_qkv_qwen3_n16k.md)
-    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69799680 + 6919168,
-                                               "source_sha": "3b72f3aa1585c90c"},
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69858560 + 6637312,
+                                               "source_sha": "9cd3022e6e5e9867"},
     "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537969920 + 3190016,
                                              "source_sha": "25e1c47fd2f58bc2"},
     "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51378432 + 24764416,
                                            "source_sha": "25e1c47fd2f58bc2"},
+    # the backward's bias-gradient kernel, M = 8432 (profiles/keybias_bias_grad_qwen3_n128k.md)
+    "qwen3_1p7b_n128k_keep6p25/keybias_bias_grad": {"bytes_per_launch": 137630464 + 3417344,
+                                                    "source_sha": "3d91e7a27c9845f8"},
 }
 
 
@@ -788,6 +791,9 @@ def run_backward(args, w, K, rank, world, local_rank):
                          "TFLOP/s": wk["flops"] / ms / 1e9 if wk["flops"] else None}
     wk, ms = work["keybias_bias_grad"], kernels["keybias_bias_grad"]["ms"]
     ach = wk["flops"] / ms / 1e9
+    trf = NCU_TRAFFIC.get(f"{w.name}/keybias_bias_grad")
+    traffic = trf["bytes_per_launch"] if trf and trf.get("source_sha") == \
+        source_hash(KERNEL_SOURCES["keybias_bias_grad"]) else None
     line = {
         "metric": "token-gated attention backward to the scorer: prompt tokens/s",
         "value": w.N / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
@@ -799,7 +805,7 @@ def run_backward(args, w, K, rank, world, local_rank):
                    "launch": "direct C-ABI calls, an event before and after each"},
         "roofline": {"kernel": "keybias_bias_grad", "bound": "tensor", "achieved": ach,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                      "algorithmic": wk["flops"], "peak_source": f"{peak_src} (bf16 burst)"},
         "kernels": kernels,
         "gpu_launches": len(calls) * steps,
