@@ -106,6 +106,16 @@ def source_hash(fname: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` at `workload` from the ncu table, or
+    None when there is no capture or the kernel's source changed since."""
+    trf = NCU_TRAFFIC.get(f"{workload}/{kernel}")
+    if trf and kernel in KERNEL_SOURCES and trf.get("source_sha") == \
+            source_hash(KERNEL_SOURCES[kernel]):
+        return trf["bytes_per_launch"]
+    return None
+
+
 # ------------------------------------------------------------ distribution --
 def dist_env() -> tuple[int, int, int]:
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
@@ -501,9 +511,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
     if dom is not None:
         wk = work[dom]
         ms = kernels[dom]["ms"]
-        trf = NCU_TRAFFIC.get(f"{w.name}/{dom}")
-        traffic = trf["bytes_per_launch"] if trf and trf.get("source_sha") == \
-            source_hash(KERNEL_SOURCES[dom]) else None
+        traffic = ncu_traffic(w.name, dom)
         if wk["bound"] == "tensor":
             ach, peak, unit = wk["flops"] / ms / 1e9, peaks["bf16_tflops"], "TFLOP/s"
         else:
@@ -791,9 +799,7 @@ def run_backward(args, w, K, rank, world, local_rank):
                          "TFLOP/s": wk["flops"] / ms / 1e9 if wk["flops"] else None}
     wk, ms = work["keybias_bias_grad"], kernels["keybias_bias_grad"]["ms"]
     ach = wk["flops"] / ms / 1e9
-    trf = NCU_TRAFFIC.get(f"{w.name}/keybias_bias_grad")
-    traffic = trf["bytes_per_launch"] if trf and trf.get("source_sha") == \
-        source_hash(KERNEL_SOURCES["keybias_bias_grad"]) else None
+    traffic = ncu_traffic(w.name, "keybias_bias_grad")
     line = {
         "metric": "token-gated attention backward to the scorer: prompt tokens/s",
         "value": w.N / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,

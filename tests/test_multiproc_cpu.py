@@ -75,3 +75,27 @@ def test_algorithmic_work_counts():
     assert work["qkv_proj"]["flops"] == 2 * M * 2048 * 4096
     assert work["gate_score"]["flops"] == 2 * 16384 * 2048 * 256
     assert work["gather_rows"]["bytes"] == 2 * M * 2048 * 2 + 12 * M
+
+
+def test_backward_work_counts_and_traffic_table():
+    sys.path.insert(0, ROOT)
+    import bench
+    w = bench.TI.WORKLOADS["qwen3_1p7b_n128k_keep6p25"]
+    M = w.M(w.Ks()[0])
+    assert M == 8432
+    bw = bench.backward_work(w, M)
+    assert set(bw) == set(bench.BWD_KERNELS)
+    # two products of 2 dh flops per causal (query, key) pair and q head
+    assert bw["keybias_bias_grad"]["flops"] == 2 * M * M * 128 * 16
+    assert bw["attn_bwd_delta"]["bytes"] == 2 * M * 16 * 128 * 2 + 16 * M * 4
+    # every ncu entry names a known kernel source; a current hash gives bytes,
+    # a stale one None
+    for key, trf in bench.NCU_TRAFFIC.items():
+        wl, kern = key.split("/")
+        assert kern in bench.KERNEL_SOURCES and wl in bench.TI.WORKLOADS
+        got = bench.ncu_traffic(wl, kern)
+        fresh = trf["source_sha"] == bench.source_hash(bench.KERNEL_SOURCES[kern])
+        assert got == (trf["bytes_per_launch"] if fresh else None)
+    assert bench.ncu_traffic(w.name, "no_such_kernel") is None
+    assert bench.ncu_traffic(w.name, "keybias_attn") is not None
+    assert bench.ncu_traffic(w.name, "keybias_bias_grad") is not None
