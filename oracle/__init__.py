@@ -17,6 +17,13 @@ Parity status per function (see the pins in ``tests/test_oracle_pins.py``):
   bias_grad_reduce        pinned (central differences of the forward, torch
                           SDPA autograd, 2-key closed form, shift invariance)
 * attn_delta              pinned (brute-force loops, softmax written out)
+* qk_rmsnorm, rope,
+  swiglu_mlp              pinned (torch rms_norm / silu / linear; rope as a
+                          complex rotation, identity at 0, norm and relative-
+                          position invariance)
+* qwen3_pruned_layer      pinned (reduces to the pinned stack layer and to the
+                          identity; kept rows at original positions = the full
+                          layer with pruned keys masked)
 * the *learned* behaviour of a trained gate (which tokens it keeps on real
   text): parity unpinned, there are no trained weights or datasets here.
 """

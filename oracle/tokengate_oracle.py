@@ -37,6 +37,12 @@ What they leave open, and the reading taken here (one line each):
   token).
 * a pruned layer of the stack: x <- x + attn(qkv(RMSNorm(x))) (no RoPE, no
   o-proj, no MLP).
+* a full decoder layer above the gate (the pages say only that the layers
+  above L process the kept tokens; their internals are the base model's):
+  Qwen3 order -- RMSNorm, q|k|v, per-head RMSNorm of q and k, rotary
+  embedding at the kept tokens' ORIGINAL prompt positions (rotate-half
+  pairing, theta_c = base^(-2c/dh)), key-bias attention, o-projection,
+  residual add, RMSNorm, SwiGLU MLP, residual add.
 * the gradient the bias carries back to the scorer ([DE] "Was ist
   token-gated Attention?": the bias gives the gradient a way back to the
   scorer; [TH] the same, MoE-router style): the plain chain rule through
@@ -53,6 +59,7 @@ import math
 
 import numpy as np
 from scipy.special import erf as _erf
+from scipy.special import expit as _expit
 
 __all__ = [
     "bf16_bits_to_f64", "f32_to_f64", "gelu_erf", "gate_score",
@@ -60,6 +67,7 @@ __all__ = [
     "logsigmoid", "gather_rows", "rmsnorm", "qkv_proj", "split_qkv",
     "keybias_attn", "gated_layer", "pruned_stack",
     "keybias_attn_lse", "attn_delta", "keybias_attn_bias_grad", "bias_grad_reduce",
+    "qk_rmsnorm", "rope", "swiglu_mlp", "qwen3_pruned_layer",
 ]
 
 
@@ -415,3 +423,78 @@ def bias_grad_reduce(dbias, logsig_kept, gain):
     dgain = dB @ ls
     ds = dls * -np.expm1(ls)
     return dls, dgain, ds
+
+
+# --------------------------------------------------------------------------
+# a full decoder layer on the kept rows ([DE] "Prune-Front-Behandlung": the
+# layers above L process only the K kept tokens; [IT] only the kept
+# representations go up).  The layer's internals are the base model's
+# (Qwen3); the one pruning-specific choice is that every kept row keeps its
+# original prompt position for the rotary embedding.
+# --------------------------------------------------------------------------
+def qk_rmsnorm(QKV, Hq: int, Hkv: int, dh: int, gamma_q, gamma_k, eps: float) -> np.ndarray:
+    """RMSNorm of every q head and every k head over its own dh columns, with
+    weights gamma_q [dh] and gamma_k [dh] shared by all heads of a kind; the
+    v columns are returned unchanged.  float64 [M][(Hq + 2 Hkv) dh]."""
+    Y = _widen(QKV).copy()
+    M = Y.shape[0]
+    for first, heads, gamma in ((0, Hq, gamma_q), (Hq, Hkv, gamma_k)):
+        blk = Y[:, first * dh:(first + heads) * dh].reshape(M, heads, dh)
+        ms = np.mean(blk * blk, axis=2, keepdims=True)
+        blk = blk / np.sqrt(ms + float(eps)) * _widen(gamma)[None, None, :]
+        Y[:, first * dh:(first + heads) * dh] = blk.reshape(M, heads * dh)
+    return Y
+
+
+def rope(QKV, Hq: int, Hkv: int, dh: int, positions, base: float) -> np.ndarray:
+    """Rotary embedding of the q and k heads: with h2 = dh / 2 and
+    theta_c = base^(-2c / dh) for c < h2, row m's pair (x_c, x_{c + h2}) of
+    every q and k head is rotated by the angle positions[m] * theta_c:
+        x_c'      = x_c cos - x_{c+h2} sin
+        x_{c+h2}' = x_{c+h2} cos + x_c sin.
+    ``positions`` are the rows' token positions in the original prompt (for
+    kept rows: the kept indices).  v unchanged.  float64."""
+    Y = _widen(QKV).copy()
+    M = Y.shape[0]
+    h2 = dh // 2
+    theta = float(base) ** (-2.0 * np.arange(h2, dtype=np.float64) / dh)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
+    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    heads = Hq + Hkv
+    blk = Y[:, :heads * dh].reshape(M, heads, dh)
+    lo, hi = blk[:, :, :h2].copy(), blk[:, :, h2:].copy()
+    blk[:, :, :h2] = lo * cos - hi * sin
+    blk[:, :, h2:] = hi * cos + lo * sin
+    Y[:, :heads * dh] = blk.reshape(M, heads * dh)
+    return Y
+
+
+def swiglu_mlp(x, Wg, Wu, Wd) -> np.ndarray:
+    """(silu(x Wg^T) * (x Wu^T)) Wd^T with silu(z) = z * sigmoid(z);
+    Wg, Wu [ffn][d], Wd [d][ffn] (nn.Linear layout)."""
+    x = _widen(x)
+    g = x @ _widen(Wg).T
+    return (g * _expit(g) * (x @ _widen(Wu).T)) @ _widen(Wd).T
+
+
+def qwen3_pruned_layer(x, positions, L: dict, Hq: int, Hkv: int, dh: int, logsig_kept,
+                       eps: float = 1e-6) -> np.ndarray:
+    """One decoder layer on the kept rows, in Qwen3's order:
+        a = RMSNorm(x; gamma_attn);  qkv = a Wqkv^T
+        qkv = rope(qk_rmsnorm(qkv; gamma_q, gamma_k), positions; rope_base)
+        x = x + keybias_attn(qkv; logsig_kept, gain, temperature) Wo^T
+        x = x + swiglu_mlp(RMSNorm(x; gamma_mlp); Wg, Wu, Wd)
+    ``L`` holds those weights.  gamma_q None skips the q/k norm, rope_base
+    None skips the rotary embedding, Wd None skips the MLP (the reductions
+    the pins use).  float64 [M][d]."""
+    x = _widen(x)
+    qkv = qkv_proj(rmsnorm(x, L["gamma_attn"], eps), L["Wqkv"])
+    if L.get("gamma_q") is not None:
+        qkv = qk_rmsnorm(qkv, Hq, Hkv, dh, L["gamma_q"], L["gamma_k"], eps)
+    if L.get("rope_base") is not None:
+        qkv = rope(qkv, Hq, Hkv, dh, positions, L["rope_base"])
+    o = keybias_attn(qkv, Hq, Hkv, dh, logsig_kept, L["gain"], L["temperature"])
+    x = x + o @ _widen(L["Wo"]).T
+    if L.get("Wd") is not None:
+        x = x + swiglu_mlp(rmsnorm(x, L["gamma_mlp"], eps), L["Wg"], L["Wu"], L["Wd"])
+    return x

@@ -641,3 +641,109 @@ def test_bias_grad_and_lse_restricted_to_the_last_keys():
     lse = O.keybias_attn_lse(QKV, Hq, Hkv, dh, ls, g, t)
     lse_p = O.keybias_attn_lse(QKV, Hq, Hkv, dh, ls, g, t, rows_from=50, chunk=9)
     np.testing.assert_allclose(lse_p[:, 50:], lse[:, 50:], rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------- a full decoder layer (NEXT-2) ---
+def test_rope_matches_complex_rotation_and_invariants():
+    Hq, Hkv, dh, M = 4, 2, 16, 9
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=51)
+    pos = np.array([0, 1, 2, 7, 100, 4095, 16383, 65535, 131071])
+    Y = O.rope(QKV, Hq, Hkv, dh, pos, 1e6)
+    h2 = dh // 2
+    theta = 1e6 ** (-np.arange(h2) * 2.0 / dh)
+    for hd in range(Hq + Hkv):                    # the same rotation as a complex product
+        z = QKV[:, hd * dh:hd * dh + h2] + 1j * QKV[:, hd * dh + h2:(hd + 1) * dh]
+        w = z * np.exp(1j * pos[:, None] * theta[None, :])
+        np.testing.assert_allclose(Y[:, hd * dh:hd * dh + h2], w.real, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(Y[:, hd * dh + h2:(hd + 1) * dh], w.imag, rtol=1e-12,
+                                   atol=1e-12)
+    np.testing.assert_array_equal(Y[0], QKV[0])                      # position 0: identity
+    np.testing.assert_array_equal(Y[:, (Hq + Hkv) * dh:], QKV[:, (Hq + Hkv) * dh:])  # v as is
+    assert np.allclose(np.linalg.norm(Y[:, :(Hq + Hkv) * dh].reshape(M, -1, dh), axis=2),
+                       np.linalg.norm(QKV[:, :(Hq + Hkv) * dh].reshape(M, -1, dh), axis=2))
+    # q.k after the rotation depends only on the distance of the positions
+    q, k = QKV[:1, :dh], QKV[1:2, Hq * dh:(Hq + 1) * dh]
+    one = np.concatenate([q, np.zeros((1, (Hq - 1) * dh)), k, np.zeros((1, (Hkv - 1 + Hkv) * dh))], 1)
+    two = np.concatenate([one, one])
+
+    def dot(pq, pk):
+        a = O.rope(two, Hq, Hkv, dh, np.array([pq, pk]), 1e6)
+        return a[0, :dh] @ a[1, Hq * dh:(Hq + 1) * dh]
+    assert abs(dot(500, 123) - dot(500 + 9999, 123 + 9999)) < 1e-9
+    assert abs(dot(500, 123) - dot(500, 124)) > 1e-6
+
+
+def test_qk_rmsnorm_matches_torch_per_head():
+    Hq, Hkv, dh, M = 4, 2, 16, 11
+    QKV = _rand_qkv(M, Hq, Hkv, dh, seed=52, scale=3.0)
+    rng = np.random.default_rng(53)
+    gq, gk = rng.uniform(0.5, 1.5, dh), rng.uniform(0.5, 1.5, dh)
+    Y = O.qk_rmsnorm(QKV, Hq, Hkv, dh, gq, gk, 1e-6)
+    t = torch.from_numpy(QKV)
+    q = F.rms_norm(t[:, :Hq * dh].reshape(M, Hq, dh), (dh,), torch.from_numpy(gq), 1e-6)
+    k = F.rms_norm(t[:, Hq * dh:(Hq + Hkv) * dh].reshape(M, Hkv, dh), (dh,),
+                   torch.from_numpy(gk), 1e-6)
+    np.testing.assert_allclose(Y[:, :Hq * dh], q.reshape(M, -1).numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(Y[:, Hq * dh:(Hq + Hkv) * dh], k.reshape(M, -1).numpy(),
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(Y[:, (Hq + Hkv) * dh:], QKV[:, (Hq + Hkv) * dh:])
+
+
+def test_swiglu_matches_torch():
+    rng = np.random.default_rng(54)
+    M, d, ffn = 7, 12, 20                      # non-square: a transposed weight fails
+    x = rng.standard_normal((M, d))
+    Wg, Wu, Wd = (rng.standard_normal(s) for s in ((ffn, d), (ffn, d), (d, ffn)))
+    t = lambda a: torch.from_numpy(a)
+    ref = F.linear(F.silu(F.linear(t(x), t(Wg))) * F.linear(t(x), t(Wu)), t(Wd)).numpy()
+    np.testing.assert_allclose(O.swiglu_mlp(x, Wg, Wu, Wd), ref, rtol=1e-12, atol=1e-12)
+    assert not O.swiglu_mlp(x, Wg, Wu, np.zeros((d, ffn))).any()
+
+
+def _layer(rng, d, Hq, Hkv, dh, ffn):
+    s = 1 / math.sqrt(d)
+    return {"gamma_attn": rng.uniform(0.9, 1.1, d), "Wqkv": rng.standard_normal(((Hq + 2 * Hkv) * dh, d)) * s,
+            "gamma_q": rng.uniform(0.9, 1.1, dh), "gamma_k": rng.uniform(0.9, 1.1, dh),
+            "rope_base": 1e6, "gain": rng.uniform(0.5, 1.5, Hq), "temperature": 1.1,
+            "Wo": rng.standard_normal((d, Hq * dh)) / math.sqrt(Hq * dh),
+            "gamma_mlp": rng.uniform(0.9, 1.1, d), "Wg": rng.standard_normal((ffn, d)) * s,
+            "Wu": rng.standard_normal((ffn, d)) * s,
+            "Wd": rng.standard_normal((d, ffn)) / math.sqrt(ffn)}
+
+
+def test_qwen3_layer_reduces_to_the_stack_layer_and_to_identity():
+    rng = np.random.default_rng(55)
+    Hq, Hkv, dh, M, ffn = 4, 2, 8, 23, 48
+    d = Hq * dh
+    x = rng.standard_normal((M, d))
+    ls = -rng.exponential(1.0, M)
+    L = _layer(rng, d, Hq, Hkv, dh, ffn)
+    # no q/k norm, no rotary embedding, Wo = I, no MLP: x + attn(qkv(RMSNorm(x)))
+    bare = dict(L, gamma_q=None, rope_base=None, Wo=np.eye(d), Wd=None)
+    stack = O.pruned_stack(x, [{"Wqkv": L["Wqkv"], "gamma": L["gamma_attn"], "gain": L["gain"],
+                                "temperature": L["temperature"]}], Hq, Hkv, dh, ls)
+    np.testing.assert_allclose(O.qwen3_pruned_layer(x, np.arange(M), bare, Hq, Hkv, dh, ls),
+                               stack, rtol=1e-12, atol=1e-12)
+    # zero output projections leave the residual stream as it is
+    zero = dict(L, Wo=np.zeros((d, Hq * dh)), Wd=np.zeros((d, ffn)))
+    np.testing.assert_array_equal(O.qwen3_pruned_layer(x, np.arange(M), zero, Hq, Hkv, dh, ls), x)
+
+
+def test_qwen3_layer_on_kept_rows_is_the_full_layer_with_pruned_keys_masked():
+    # the kept rows, each at its original position, give exactly what the full
+    # prompt's layer gives at those rows when every pruned key is masked out
+    rng = np.random.default_rng(56)
+    Hq, Hkv, dh, N, ffn = 4, 2, 8, 40, 32
+    d = Hq * dh
+    x = rng.standard_normal((N, d))
+    ls = -rng.exponential(1.0, N)
+    L = _layer(rng, d, Hq, Hkv, dh, ffn)
+    idx = np.array([0, 3, 4, 9, 17, 18, 25, 31] + list(range(34, 40)))
+    masked = np.full(N, -np.inf)
+    masked[idx] = ls[idx]
+    full = O.qwen3_pruned_layer(x, np.arange(N), L, Hq, Hkv, dh, masked)
+    kept = O.qwen3_pruned_layer(x[idx], idx, L, Hq, Hkv, dh, ls[idx])
+    np.testing.assert_allclose(kept, full[idx], rtol=1e-11, atol=1e-12)
+    # and the positions matter: compacted positions give a different result
+    other = O.qwen3_pruned_layer(x[idx], np.arange(idx.size), L, Hq, Hkv, dh, ls[idx])
+    assert np.abs(other - kept).max() > 1e-3
