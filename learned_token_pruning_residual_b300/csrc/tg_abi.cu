@@ -8,6 +8,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 
 #include "tg_device.cuh"
@@ -118,6 +120,17 @@ tg_status from_cuda(cudaError_t e, const char* what) {
   return fail(TG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// An NVTX range around one C-ABI call (named after the call), so that
+// profilers show which call launched which kernels (e.g. ncu --nvtx
+// --nvtx-include "tg_keybias_attn/"); a no-op unless a tool is attached.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define TG_TRACE_CALL() CallRange tg_call_range_(__func__)
+
 #define TG_REQUIRE(cond, code, ...) \
   do {                              \
     if (!(cond)) return fail(code, __VA_ARGS__); \
@@ -181,6 +194,7 @@ const char* tg_last_error_message(void) { return tg::t_last_error; }
 tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d, const void* W1,
                         const float* b1, int32_t Hg, const float* w2, float b2, float* scores,
                         tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "gate: bad dtype");
   TG_REQUIRE(N >= 0 && N < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "gate: N out of range");
   TG_REQUIRE(d > 0 && Hg > 0, TG_ERR_INVALID_ARG, "gate: d and Hg must be positive");
@@ -206,6 +220,7 @@ tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d, con
 
 tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin, int64_t doc_end,
                          int64_t K, int32_t* kept_idx, int64_t* M_out, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(N >= 0 && N < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "select: N out of range");
   TG_REQUIRE(0 <= doc_begin && doc_begin <= doc_end && doc_end <= N, TG_ERR_INVALID_ARG,
              "select: need 0 <= doc_begin <= doc_end <= N");
@@ -225,6 +240,7 @@ tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin, int6
 tg_status tg_gather_rows(const void* X, tg_dtype x_dtype, int64_t N, int32_t d,
                          const int32_t* idx, int64_t M, void* Y, tg_dtype y_dtype,
                          const float* scores, float* logsig_kept, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE((x_dtype == TG_BF16 && (y_dtype == TG_BF16 || y_dtype == TG_F32)) ||
                  (x_dtype == TG_F32 && y_dtype == TG_F32),
              TG_ERR_UNSUPPORTED, "gather: dtype pair not supported");
@@ -246,6 +262,7 @@ tg_status tg_gather_rows(const void* X, tg_dtype x_dtype, int64_t N, int32_t d,
 
 tg_status tg_rmsnorm(const void* X, tg_dtype x_dtype, int64_t M, int32_t d, const float* gamma,
                      float eps, void* Y, tg_dtype y_dtype, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE((x_dtype == TG_F32 || x_dtype == TG_BF16) && (y_dtype == TG_F32 || y_dtype == TG_BF16),
              TG_ERR_INVALID_ARG, "rmsnorm: bad dtype");
   TG_REQUIRE(M >= 0 && d > 0 && d % 8 == 0, TG_ERR_INVALID_ARG, "rmsnorm: need d %% 8 == 0");
@@ -261,6 +278,7 @@ tg_status tg_rmsnorm(const void* X, tg_dtype x_dtype, int64_t M, int32_t d, cons
 
 tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d, const void* Wqkv,
                       int32_t Hq, int32_t Hkv, int32_t dh, void* QKV, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "qkv: bad dtype");
   TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && d > 0 && Hq > 0 && Hkv > 0 && dh > 0,
              TG_ERR_INVALID_ARG, "qkv: bad sizes");
@@ -287,6 +305,7 @@ tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d, const
 tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq, int32_t Hkv,
                           int32_t dh, const float* logsig_kept, const float* gain,
                           float temperature, void* O, float* residual, tg_stream_t stream) {
+  TG_TRACE_CALL();
   return keybias_attn_impl(QKV, dtype, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
                            residual, nullptr, stream);
 }
@@ -295,6 +314,7 @@ tg_status tg_keybias_attn_lse(const void* QKV, tg_dtype dtype, int64_t M, int32_
                               int32_t Hkv, int32_t dh, const float* logsig_kept,
                               const float* gain, float temperature, void* O, float* residual,
                               float* lse, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(lse || M == 0, TG_ERR_INVALID_ARG, "attn lse: NULL lse");
   return keybias_attn_impl(QKV, dtype, M, Hq, Hkv, dh, logsig_kept, gain, temperature, O,
                            residual, lse, stream);
@@ -302,6 +322,7 @@ tg_status tg_keybias_attn_lse(const void* QKV, tg_dtype dtype, int64_t M, int32_
 
 tg_status tg_attn_bwd_delta(const void* dO, const void* O, tg_dtype dtype, int64_t M, int32_t Hq,
                             int32_t dh, float* delta, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "delta: bad dtype");
   TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && dh > 0, TG_ERR_INVALID_ARG,
              "delta: bad sizes");
@@ -322,6 +343,7 @@ tg_status tg_keybias_attn_bias_grad(const void* QKV, const void* dO, tg_dtype dt
                                     const float* logsig_kept, const float* gain,
                                     float temperature, const float* lse, const float* delta,
                                     float* dbias, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "bias grad: bad dtype");
   TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0 && Hkv > 0 && dh > 0,
              TG_ERR_INVALID_ARG, "bias grad: bad sizes");
@@ -353,6 +375,7 @@ tg_status tg_keybias_attn_bias_grad(const void* QKV, const void* dO, tg_dtype dt
 tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
                               const float* logsig_kept, const float* gain, float* dlogsig,
                               float* dgain, float* dscore, tg_stream_t stream) {
+  TG_TRACE_CALL();
   TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && Hq > 0, TG_ERR_INVALID_ARG,
              "bias grad reduce: bad sizes");
   TG_REQUIRE(dgain && gain, TG_ERR_INVALID_ARG, "bias grad reduce: NULL pointer");
