@@ -329,6 +329,9 @@ tg_status tg_attn_bwd_delta(const void* dO, const void* O, tg_dtype dtype, int64
   TG_REQUIRE(dtype == TG_BF16 ? (dh == 64 || dh == 128 || dh == 256)
                               : (dh == 32 || dh == 64 || dh == 128),
              TG_ERR_UNSUPPORTED, "delta: dh must be 64, 128 or 256 (bf16), 32, 64 or 128 (f32)");
+  // one thread per 16-byte chunk, 256 a block: the grid must fit in 2^31 - 1
+  TG_REQUIRE(M * Hq * (dh * (dtype == TG_BF16 ? 2 : 4) / 16) / 256 < (int64_t(1) << 31) - 1,
+             TG_ERR_UNSUPPORTED, "delta: M * Hq too large");
   if (M == 0) return TG_OK;
   TG_REQUIRE(dO && O && delta, TG_ERR_INVALID_ARG, "delta: NULL pointer");
   TG_REQUIRE(aligned16(dO) && aligned16(O) && aligned16(delta), TG_ERR_INVALID_ARG,

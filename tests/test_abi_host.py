@@ -132,6 +132,7 @@ def test_backward_argument_errors(L):
     assert L.tg_attn_bwd_delta(p, None, 1, 10, 16, 128, p, None) == 1
     assert L.tg_attn_bwd_delta(p, odd, 1, 10, 16, 128, p, None) == 1
     assert L.tg_attn_bwd_delta(None, None, 1, 0, 16, 128, None, None) == 0
+    assert L.tg_attn_bwd_delta(p, p, 1, 2**31 - 1, 4096, 256, p, None) == 2   # grid too large
     # bias gradient
     args = lambda **kw: [kw.get("qkv", p), kw.get("do", p), kw.get("dt", 1), kw.get("M", 10),
                          kw.get("Hq", 16), kw.get("Hkv", 8), kw.get("dh", 128), kw.get("ls", p),
