@@ -362,6 +362,8 @@ tg_status tg_keybias_attn_bias_grad(const void* QKV, const void* dO, tg_dtype dt
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == TG_BF16) {
     TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "bias grad bf16: dh must be 128");
+    TG_REQUIRE((M + 127) / 128 * Hq < (int64_t(1) << 31) - 1, TG_ERR_UNSUPPORTED,
+               "bias grad bf16: (M / 128) * Hq blocks exceed the grid limit");
     return from_cuda(tg::launch_bias_grad_bf16(QKV, dO, M, Hq, Hkv, dh, logsig_kept, gain,
                                                temperature, lse, delta, dbias, st),
                      "bias grad bf16");

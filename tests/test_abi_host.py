@@ -148,6 +148,7 @@ def test_backward_argument_errors(L):
     assert L.tg_keybias_attn_bias_grad(*args(dh=64)) == 2                 # bf16 needs dh 128
     assert L.tg_keybias_attn_bias_grad(*args(dt=0, dh=96)) == 2
     assert L.tg_keybias_attn_bias_grad(*args(M=0, qkv=None, do=None)) == 0
+    assert L.tg_keybias_attn_bias_grad(*args(M=2**31 - 1, Hq=2**16, Hkv=2**15)) == 2
     # reduction
     assert L.tg_bias_grad_reduce(p, 10, 0, p, p, p, p, None, None) == 1     # Hq
     assert L.tg_bias_grad_reduce(p, 10, 4, None, p, p, p, None, None) == 1  # logsig
