@@ -267,9 +267,31 @@ tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
  * Synchronises `stream`, then returns and clears the sticky device status
  * of the current device: TG_OK, or the first of TG_ERR_NAN_SCORE,
  * TG_ERR_BAD_INDEX, TG_ERR_TIMEOUT that is set.  TG_ERR_CUDA if the
- * synchronisation itself failed.
+ * synchronisation itself failed.  The word is per device and shared by all
+ * streams; it is read and cleared in one atomic exchange on `stream`, so a
+ * bit that a kernel on another stream sets meanwhile is either returned now
+ * or kept for the next call, never lost.
  */
 tg_status tg_get_device_status(tg_stream_t stream);
+
+/*
+ * Self-check of the failure path (the pages have no counterpart: this is the
+ * library's own diagnostic).  Every pipeline wait in this library is bounded:
+ * a wait that gives up sets TG_ERR_TIMEOUT in the device status word and an
+ * abort flag that makes the CTA's other waiters leave, so a lost arrival
+ * becomes an error status instead of a hung GPU.  This call launches one CTA
+ * with an mbarrier that nothing completes: one thread waits on it with a
+ * bound of `timeout_us` microseconds and gives up; a second thread waits on
+ * it with the pipelines' own bound (2 s) and must leave early because of the
+ * abort flag.  Afterwards tg_get_device_status returns TG_ERR_TIMEOUT (once),
+ * and the device stays usable.
+ *  timeout_us  1 .. 1000000.
+ *  report      device, 4 x uint64, or NULL: for the short-bound waiter then
+ *              the abort-driven waiter, (1 if its wait succeeded else 0,
+ *              nanoseconds it waited).  8-byte aligned.
+ */
+tg_status tg_selftest_bounded_wait(uint32_t timeout_us, unsigned long long* report,
+                                   tg_stream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

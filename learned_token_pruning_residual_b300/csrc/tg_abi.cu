@@ -20,6 +20,14 @@ namespace tg {
 // The sticky per-device status word.  Kernels OR error bits into it;
 // tg_get_device_status reads and clears it.
 __device__ uint32_t g_status_word = 0;
+// Where tg_get_device_status takes the word to (read and cleared in one
+// atomic exchange, so a bit that a kernel on another stream sets at the same
+// time is either taken now or left for the next read, never lost).
+__device__ uint32_t g_status_taken = 0;
+
+__global__ void status_take_kernel(uint32_t* status, uint32_t* taken) {
+  *taken = atomicExch(status, 0u);
+}
 
 namespace {
 thread_local char t_last_error[512] = "";
@@ -68,6 +76,17 @@ uint32_t* device_status_word() {
     g_status_ptr[dev] = static_cast<uint32_t*>(p);
   }
   return g_status_ptr[dev];
+}
+
+cudaError_t launch_status_take(uint32_t** taken, cudaStream_t stream) {
+  uint32_t* status = device_status_word();
+  if (status == nullptr) return cudaErrorInvalidDevice;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_status_taken);
+  if (e != cudaSuccess) return e;
+  *taken = static_cast<uint32_t*>(p);
+  status_take_kernel<<<1, 1, 0, stream>>>(status, *taken);
+  return cudaGetLastError();
 }
 
 int sm_count() {
@@ -329,7 +348,10 @@ tg_status tg_attn_bwd_delta(const void* dO, const void* O, tg_dtype dtype, int64
   TG_REQUIRE(dtype == TG_BF16 ? (dh == 64 || dh == 128 || dh == 256)
                               : (dh == 32 || dh == 64 || dh == 128),
              TG_ERR_UNSUPPORTED, "delta: dh must be 64, 128 or 256 (bf16), 32, 64 or 128 (f32)");
-  // one thread per 16-byte chunk, 256 a block: the grid must fit in 2^31 - 1
+  // one thread per 16-byte chunk, 256 a block: the grid must fit in 2^31 - 1.
+  // With M < 2^31, Hq <= 2^16 and at most 32 chunks a head the product stays
+  // below 2^52, so it cannot overflow.
+  TG_REQUIRE(Hq <= 65536, TG_ERR_UNSUPPORTED, "delta: Hq > 65536");
   TG_REQUIRE(M * Hq * (dh * (dtype == TG_BF16 ? 2 : 4) / 16) / 256 < (int64_t(1) << 31) - 1,
              TG_ERR_UNSUPPORTED, "delta: M * Hq too large");
   if (M == 0) return TG_OK;
@@ -395,23 +417,35 @@ tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
 }
 
 tg_status tg_get_device_status(tg_stream_t stream) {
+  static std::mutex take_mu;  // one taker at a time per process (one g_status_taken per device)
+  std::lock_guard<std::mutex> lk(take_mu);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
-  uint32_t* p = tg::device_status_word();
-  if (!p) return fail(TG_ERR_CUDA, "status: no device status word");
-  uint32_t v = 0;
-  e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  uint32_t* taken = nullptr;
+  e = tg::launch_status_take(&taken, st);
   if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
-  if (v != 0) {
-    const uint32_t zero = 0;
-    e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
-  }
+  uint32_t v = 0;
+  e = cudaMemcpyAsync(&v, taken, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(TG_ERR_CUDA, "status: %s", cudaGetErrorString(e));
   if (v & tg::kStatusNanScore) return TG_ERR_NAN_SCORE;
   if (v & tg::kStatusBadIndex) return TG_ERR_BAD_INDEX;
   if (v & tg::kStatusTimeout) return TG_ERR_TIMEOUT;
   return TG_OK;
+}
+
+tg_status tg_selftest_bounded_wait(uint32_t timeout_us, unsigned long long* report,
+                                   tg_stream_t stream) {
+  TG_TRACE_CALL();
+  TG_REQUIRE(timeout_us >= 1 && timeout_us <= 1000000, TG_ERR_INVALID_ARG,
+             "selftest: need 1 <= timeout_us <= 1000000");
+  TG_REQUIRE(!report || (reinterpret_cast<uintptr_t>(report) & 7u) == 0, TG_ERR_INVALID_ARG,
+             "selftest: report must be 8-byte aligned");
+  return from_cuda(tg::launch_bounded_wait_selftest(static_cast<uint64_t>(timeout_us) * 1000ull,
+                                                    report,
+                                                    reinterpret_cast<cudaStream_t>(stream)),
+                   "selftest");
 }
 
 }  // extern "C"

@@ -82,21 +82,27 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 constexpr uint32_t kWaitSleepNs = 20000;  // 20 us
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up
-// when *abort is set by another thread, or after kWaitTimeoutNs (then sets
+// when *abort is set by another thread, or after `timeout_ns` (then sets
 // *abort and the device status).  Returns false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              uint32_t* status, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
       *abort = 1;
       if (status) atomicOr(status, kStatusTimeout);
       return false;
     }
   }
+}
+
+// The pipelines' wait: mbar_wait_for with the library-wide bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  return mbar_wait_for(bar, parity, abort, status, kWaitTimeoutNs);
 }
 
 // Same, ignoring the abort flag (used in teardown to drain copies that are

@@ -97,4 +97,10 @@ cudaError_t launch_bias_grad_reduce(const float* dbias, int64_t M, int Hq, const
                                     const float* gain, float* dls, float* dgain, float* dscore,
                                     cudaStream_t stream);
 
+cudaError_t launch_bounded_wait_selftest(uint64_t timeout_ns, unsigned long long* report,
+                                         cudaStream_t stream);
+// Reads and clears the status word in one atomic step on `stream`, into a
+// device word whose address is returned through *taken.
+cudaError_t launch_status_take(uint32_t** taken, cudaStream_t stream);
+
 }  // namespace tg

@@ -18,6 +18,7 @@ Functions carry the C names:
     tg_keybias_attn_bias_grad  dL/db for the per-head key bias b = g_h * logsig
     tg_bias_grad_reduce        dL/dlogsig, dL/dgain and dL/dscore from dL/db
     tg_get_device_status
+    tg_selftest_bounded_wait   a wait that must give up (the failure path)
 
 plus three compositions of them, ``gated_layer``, ``pruned_stack`` and
 ``bias_backward``.
@@ -33,7 +34,7 @@ __all__ = [
     "TokenGateError", "lib", "library_path", "TG_F32", "TG_BF16",
     "tg_gate_score", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
     "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
-    "tg_bias_grad_reduce", "tg_get_device_status", "gated_layer", "pruned_stack",
+    "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait", "gated_layer", "pruned_stack",
     "bias_backward", "EXPORTED_SYMBOLS",
 ]
 
@@ -63,6 +64,7 @@ _SIGNATURES = {
                                   _p, _p, _p],
     "tg_bias_grad_reduce": [_p, _i64, _i32, _p, _p, _p, _p, _p, _p],
     "tg_get_device_status": [_p],
+    "tg_selftest_bounded_wait": [ctypes.c_uint32, _p, _p],
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -248,6 +250,15 @@ def tg_get_device_status(raise_on_error: bool = True) -> int:
     if raise_on_error:
         _check(st)
     return st
+
+
+def tg_selftest_bounded_wait(timeout_us: int, report=None) -> None:
+    """Launch the failure-path self-check (one CTA waits on an mbarrier that
+    nothing completes and gives up after timeout_us).  ``report`` (uint64
+    [4] on the device, optional) receives (ok, ns) of the short-bound waiter
+    and of the abort-driven waiter.  Read the result with
+    tg_get_device_status(raise_on_error=False): it returns TG_ERR_TIMEOUT."""
+    _check(lib().tg_selftest_bounded_wait(int(timeout_us), _ptr(report), _stream()))
 
 
 def gated_layer(X, W1, b1, w2, b2, doc_begin, doc_end, K, Wqkv, Hq, Hkv, dh, gain, temperature,

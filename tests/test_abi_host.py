@@ -154,3 +154,10 @@ def test_backward_argument_errors(L):
     assert L.tg_bias_grad_reduce(p, 10, 4, None, p, p, p, None, None) == 1  # logsig
     assert L.tg_bias_grad_reduce(p, 10, 4, p, p, p, None, None, None) == 1  # dgain
     assert L.tg_bias_grad_reduce(p, 10, 4, p, p, p, p, odd, None) == 1      # dscore alignment
+
+
+def test_selftest_bounded_wait_argument_errors(L):
+    assert L.tg_selftest_bounded_wait(0, None, None) == 1            # timeout 0
+    assert L.tg_selftest_bounded_wait(1000001, None, None) == 1      # longer than 1 s
+    assert b"timeout_us" in L.tg_last_error_message()
+    assert L.tg_selftest_bounded_wait(100, ctypes.c_void_p(0x1004), None) == 1  # misaligned report

@@ -11,8 +11,8 @@ import oracle as O
 import tg_inputs as TI
 from learned_token_pruning_residual_b300 import build as tgbuild
 import learned_token_pruning_residual_b300 as tg
-from gpu_helpers import (GATE_REL, assert_attn_close, assert_gate_close, assert_stack_close, f64,
-                         to_dev)
+from gpu_helpers import (GATE_REL, assert_attn_close, assert_gate_close,
+                         assert_stack_drift_sane, f64, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +62,9 @@ def _run_chain(w, K, X, gp, Wqkv, ap, rows=None):
     s_orc = O.gate_score(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"])
     assert_gate_close(f64(out["scores"]), s_orc)
     gpu_idx = out["idx"].cpu().numpy()
+    # the bit-exact contract: the same fp32 score vector gives the same indices
+    gpu_s32 = out["scores"].cpu().numpy()
+    assert np.array_equal(gpu_idx, O.select_topk(gpu_s32, w.doc_begin, w.doc_end, K))
     ref_idx, same = _check_selection(gpu_idx, s_orc, w.doc_begin, w.doc_end, K)
     if not same:  # run the GPU downstream on the oracle's selection
         Xk, ls = tg.tg_gather_rows(Xd, to_dev(ref_idx.astype(np.int32)), out["scores"])
@@ -164,10 +167,58 @@ def test_64k_stack_one_layer_full_rows():
     assert_attn_close(f64(x)[rows], ref)
 
 
-def test_stack_20_layers_small_rows():
-    """All 20 layers end to end (no teacher forcing) at a reduced row count,
-    against the untethered fp64 stack.  The errors of 20 bf16 layers
-    accumulate; the bound is sqrt(20) times the attention tolerance."""
+def test_64k_stack20_teacher_forced_every_layer():
+    """The pruned-stack workload at its stated size, end to end on the GPU:
+    gate over N = 65536 tokens, select (bit-exact on the GPU's own scores),
+    gather of the M = 6784 kept rows into the fp32 residual stream, then all
+    20 layers.  Every layer is teacher-forced: the oracle takes the GPU's own
+    input of that layer and computes RMSNorm -> QKV -> key-bias attention ->
+    residual add on 1024 sampled rows plus the 256 question rows, which must
+    match the GPU's output of the layer at the attention tolerance
+    (2e-2 max-abs, 1e-2 mean-abs), unrelaxed."""
+    w = TI.WORKLOADS["qwen3_1p7b_n64k_stack20_keep10"]
+    K = w.Ks()[0]
+    M = w.M(K)
+    X = TI.residual(w)
+    gp = TI.gate_params(w)
+    Xd = to_dev(X)
+    s = tg.tg_gate_score(Xd, to_dev(gp["W1"]), to_dev(gp["b1"]), to_dev(gp["w2"]), gp["b2"])
+    assert_gate_close(f64(s), O.gate_score(X, gp["W1"], gp["b1"], gp["w2"], gp["b2"]))
+    idx = tg.tg_select_topk(s, w.doc_begin, w.doc_end, K)
+    s32 = s.cpu().numpy()
+    ref_idx = O.select_topk(s32, w.doc_begin, w.doc_end, K)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    x = torch.empty(M, w.d, dtype=torch.float32, device=Xd.device)
+    _, ls = tg.tg_gather_rows(Xd, idx, s, out=x)
+    x_ref, ls_ref = O.gather_rows(X, ref_idx, s32)
+    assert np.array_equal(f64(x), x_ref)
+    np.testing.assert_allclose(f64(ls), ls_ref, rtol=2e-6, atol=1e-7)
+    del Xd
+    layers = _stack_layers(w, w.layers)
+    dlayers = _dev_layers(layers)
+    rows = _sample_rows(M, 1024, seed=64)
+    worst = (0.0, 0.0)
+    for li, (L, Ld) in enumerate(zip(layers, dlayers)):
+        x_in = x.cpu().numpy()  # the GPU's input of this layer, fp32
+        tg.pruned_stack(x, [Ld], w.Hq, w.Hkv, w.dh, ls)
+        got = f64(x)[rows]
+        qkv = O.qkv_proj(O.rmsnorm(x_in, L["gamma"], 1e-6), L["Wqkv"])
+        ref = x_in[rows].astype(np.float64) + O.keybias_attn(
+            qkv, w.Hq, w.Hkv, w.dh, f64(ls), L["gain"], L["temperature"], rows=rows)
+        mx, mean = assert_attn_close(got, ref)
+        worst = (max(worst[0], mx), max(worst[1], mean))
+    assert tg.tg_get_device_status(raise_on_error=False) == 0
+    print(f"64k stack, 20 layers teacher-forced: worst layer max-abs {worst[0]:.2e} "
+          f"mean-abs {worst[1]:.2e}")
+
+
+def test_stack_20_layers_untethered_drift_report():
+    """Information only, not a parity claim: all 20 layers end to end with
+    no teacher forcing, at a reduced row count the fp64 stack finishes in
+    seconds.  The bf16 roundings of each layer carry into the next one's
+    input, so the gap to the untethered fp64 stack grows with depth; the
+    check is a sanity bound (sqrt(20) times the attention tolerance), and
+    the printed figures are the drift."""
     w = TI.WORKLOADS["qwen3_1p7b_n64k_stack20_keep10"]
     M = 640
     x0 = np.random.default_rng(9).standard_normal((M, w.d)).astype(np.float32)
@@ -176,5 +227,5 @@ def test_stack_20_layers_small_rows():
     x = to_dev(x0)
     tg.pruned_stack(x, _dev_layers(layers), w.Hq, w.Hkv, w.dh, to_dev(ls))
     ref = O.pruned_stack(x0, layers, w.Hq, w.Hkv, w.dh, ls)
-    mx, mean = assert_stack_close(f64(x), ref, w.layers)
-    print(f"20-layer stack: max-abs {mx:.2e} mean-abs {mean:.2e}")
+    mx, mean = assert_stack_drift_sane(f64(x), ref, w.layers)
+    print(f"20-layer stack drift (untethered, M={M}): max-abs {mx:.2e} mean-abs {mean:.2e}")
