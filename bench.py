@@ -369,12 +369,14 @@ def run_gpu(args, w, K, rank, world, local_rank):
                 "Xk": torch.empty(M, w.d, dtype=bf, device=dev),
                 "ls": torch.empty(M, dtype=torch.float32, device=dev),
                 "qkv": torch.empty(M, w.qkv_cols, dtype=bf, device=dev),
-                "out": torch.empty(M, w.Hq * w.dh, dtype=bf, device=dev)}
+                "out": torch.empty(M, w.Hq * w.dh, dtype=bf, device=dev),
+                "ws": tg.new_select_workspace(dev)}
 
     A = make_bufs(to_dev(X_host))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     m_out = ctypes.c_int64(0)
+    ws_bytes = tg.tg_select_workspace_bytes()
     t = ap["temperature"]
     wp = {"W1": W1.data_ptr(), "b1": b1.data_ptr(), "w2": w2.data_ptr(),
           "Wqkv": Wqkv.data_ptr(), "gain": gain.data_ptr()}
@@ -389,9 +391,10 @@ def run_gpu(args, w, K, rank, world, local_rank):
         p = {k: v.data_ptr() for k, v in bufs.items()}
         return [
             lambda: check(L.tg_gate_score(p["X"], 1, w.N, w.d, wp["W1"], wp["b1"], w.Hg,
-                                          wp["w2"], gp["b2"], p["s"], sh)),
+                                          wp["w2"], gp["b2"], p["s"], p["ws"], w.doc_begin,
+                                          w.doc_end, sh)),
             lambda: check(L.tg_select_topk(p["s"], w.N, w.doc_begin, w.doc_end, K, p["idx"],
-                                           ctypes.byref(m_out), sh)),
+                                           ctypes.byref(m_out), p["ws"], ws_bytes, sh)),
             lambda: check(L.tg_gather_rows(p["X"], 1, w.N, w.d, p["idx"], M, p["Xk"], 1,
                                            p["s"], p["ls"], sh)),
             lambda: check(L.tg_qkv_proj(p["Xk"], 1, M, w.d, wp["Wqkv"], w.Hq, w.Hkv, w.dh,
@@ -679,7 +682,8 @@ def run_compare(args, w, K, rank, world, local_rank):
         b = {"scores": torch.empty(w.N, dtype=f32, device=dev),
              "idx": torch.empty(M, dtype=torch.int32, device=dev),
              "logsig": torch.empty(M, dtype=f32, device=dev),
-             "qkv": torch.empty(M, w.qkv_cols, dtype=bf, device=dev)}
+             "qkv": torch.empty(M, w.qkv_cols, dtype=bf, device=dev),
+             "ws": tg.new_select_workspace(dev)}
         if stack:
             b["x"] = torch.empty(M, w.d, dtype=f32, device=dev)
             b["xn"] = torch.empty(M, w.d, dtype=bf, device=dev)
@@ -698,8 +702,9 @@ def run_compare(args, w, K, rank, world, local_rank):
         return b
 
     def gated(b):
-        s = tg.tg_gate_score(X, W1, b1, w2, gp["b2"], out=b["scores"])
-        idx = tg.tg_select_topk(s, w.doc_begin, w.doc_end, K, out=b["idx"])
+        s = tg.tg_gate_score(X, W1, b1, w2, gp["b2"], out=b["scores"], select_ws=b["ws"],
+                             doc_begin=w.doc_begin, doc_end=w.doc_end)
+        idx = tg.tg_select_topk(s, w.doc_begin, w.doc_end, K, out=b["idx"], workspace=b["ws"])
         if stack:
             tg.tg_gather_rows(X, idx, s, out=b["x"], logsig_out=b["logsig"])
             tg.pruned_stack(b["x"], layers, w.Hq, w.Hkv, w.dh, b["logsig"],

@@ -66,7 +66,7 @@ typedef enum tg_dtype { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
 const char* tg_status_string(int status);
 
 /* ABI version of this header (bumped on any signature change). */
-#define TG_ABI_VERSION 2
+#define TG_ABI_VERSION 3
 int tg_abi_version(void);
 
 /* Message of the last TG_ERR_INVALID_ARG / TG_ERR_UNSUPPORTED / TG_ERR_CUDA
@@ -87,14 +87,39 @@ const char* tg_last_error_message(void);
  *  b1      [Hg] fp32, or NULL for zero.
  *  w2      [Hg] fp32.   b2: scalar.
  *  scores  [N] fp32 output.
+ *  select_ws, doc_begin, doc_end: optional fusion with the next
+ *          tg_select_topk.  When select_ws (a select workspace, see below)
+ *          is given on the TG_BF16 path, the epilogue that produces the
+ *          scores also counts the first radix pass of the selection (the top
+ *          11 bits of each score key in [doc_begin, doc_end)) into it and
+ *          stamps it with (N, doc_begin, doc_end); a tg_select_topk on the
+ *          same span and workspace then skips that pass.  NULL: no fusion
+ *          (doc_begin, doc_end ignored).  TG_F32 ignores the workspace.
  * Limits: N >= 0 (N == 0 launches nothing); d % 64 == 0 for TG_BF16
  * (d % 4 == 0 for TG_F32); 16 <= Hg <= 256 and Hg % 16 == 0 for TG_BF16,
- * 1 <= Hg <= 1024 for TG_F32.
+ * 1 <= Hg <= 1024 for TG_F32; with select_ws, 0 <= doc_begin <= doc_end <= N.
  */
 tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d,
                         const void* W1, const float* b1, int32_t Hg,
                         const float* w2, float b2, float* scores,
+                        void* select_ws, int64_t doc_begin, int64_t doc_end,
                         tg_stream_t stream);
+
+/*
+ * Bytes of the select workspace (device memory the caller owns, 256-byte
+ * aligned, used by tg_select_topk and optionally filled by tg_gate_score):
+ * 40 KiB for any N.  It must be zeroed once before its first use
+ * (cudaMemset); every tg_select_topk that returns TG_OK and whose kernel
+ * finishes without a device error leaves it ready for the next call: its
+ * histograms (including one a tg_gate_score put there), header and barrier
+ * counter are back at zero (per-CTA counts and a barrier generation word
+ * carry over and need no reset), so it can be reused call after call on
+ * one stream.  A tg_gate_score that filled it must be followed by a
+ * tg_select_topk on the same workspace before the next tg_gate_score.
+ * After TG_ERR_TIMEOUT, zero it again.  Calls that share a workspace must
+ * not overlap on the GPU (use one workspace per stream).
+ */
+size_t tg_select_workspace_bytes(int64_t N);
 
 /*
  * Top-K select ([DE] same section: after scoring, the gate keeps the K
@@ -107,18 +132,23 @@ tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d,
  * indices to kept_idx in ascending order.  The result is unique, so the
  * call is deterministic and bit-exact.
  *
- *  scores    [N] fp32.
- *  kept_idx  [M] int32 output, M = N - (doc_end - doc_begin) + K.
- *  M_out     host pointer (nullable): receives M, computed on the host, so
- *            no device synchronisation is needed to size the next calls.
+ *  scores     [N] fp32.
+ *  kept_idx   [M] int32 output, M = N - (doc_end - doc_begin) + K.
+ *  M_out      host pointer (nullable): receives M, computed on the host, so
+ *             no device synchronisation is needed to size the next calls.
+ *  workspace  device, workspace_bytes >= tg_select_workspace_bytes(N),
+ *             256-byte aligned, zeroed before its first use (see above).
  * Limits: 0 <= doc_begin <= doc_end <= N < 2^31, 0 <= K <= doc_end -
  * doc_begin.  M == 0 launches nothing.  A NaN score inside the span sets
  * TG_ERR_NAN_SCORE in the device status word (NaN then ranks above +inf).
- * One 8-CTA cluster does the whole selection; no workspace is needed.
+ * One launch of up to one CTA per SM (about 4096 keys each); the CTAs meet
+ * at grid barriers in the workspace whose waits are bounded (a barrier that
+ * never completes sets TG_ERR_TIMEOUT instead of hanging).
  */
 tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin,
                          int64_t doc_end, int64_t K, int32_t* kept_idx,
-                         int64_t* M_out, tg_stream_t stream);
+                         int64_t* M_out, void* workspace, size_t workspace_bytes,
+                         tg_stream_t stream);
 
 /*
  * Row gather ([IT] "TokenGate impara quali token mantenere": only the kept

@@ -45,6 +45,8 @@ struct GemmArgs {
   const float* w2;
   float b2;
   float* scores;
+  SelectWorkspace* sel_ws;  // EPI_GATE, nullable: first radix histogram of the span's keys
+  int doc_b, doc_e;
   uint32_t* status;
 };
 
@@ -73,8 +75,9 @@ __device__ __forceinline__ float gelu_as(float z) {
 // quadrant, column halves chalf, partial sums met in `part`).
 template <int BN, int EPI, int kEpiWarps>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, const float* b1s,
-                                              const float* w2s, float* part, uint32_t tmem_acc,
-                                              int tm, int tn, int r_in_tile, int q, int chalf) {
+                                              const float* w2s, float* part, uint32_t* hist,
+                                              uint32_t tmem_acc, int tm, int tn, int r_in_tile,
+                                              int q, int chalf) {
   const int64_t row = static_cast<int64_t>(tm) * BM + r_in_tile;
   const bool row_ok = row < args.M;
   const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
@@ -121,7 +124,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, const float*
     }
     if (chalf == 1) part[r_in_tile] = acc;
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-    if (chalf == 0 && row_ok) args.scores[row] = acc + part[r_in_tile] + args.b2;
+    if (chalf == 0) {
+      const float s = acc + part[r_in_tile] + args.b2;
+      if (row_ok) args.scores[row] = s;
+      if (args.sel_ws != nullptr) {
+        // first radix pass of the select: top 11 bits of the score's key,
+        // for document rows only; warp-aggregated shared-memory counts
+        uint32_t bin = 0xFFFFFFFFu;
+        if (row_ok && row >= args.doc_b && row < args.doc_e) {
+          const uint32_t u = __float_as_uint(s);
+          bin = ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) >> 21;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (bin != 0xFFFFFFFFu && (threadIdx.x & 31) == __ffs(peers) - 1)
+          atomicAdd(hist + bin, __popc(peers));
+      }
+    }
   }
 }
 
@@ -148,6 +166,7 @@ struct PairSmem {
   float b1[256];
   float w2[256];
   float part[2][BM];
+  uint32_t hist[2048];  // gate: first radix histogram of this CTA's document rows
 };
 
 template <int BN, int STAGES, int EPI>
@@ -281,6 +300,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         S.b1[i] = (i < args.N && args.b1 != nullptr) ? args.b1[i] : 0.f;
         S.w2[i] = (i < args.N) ? args.w2[i] : 0.f;
       }
+      if (args.sel_ws != nullptr)
+        for (int i = threadIdx.x - 64; i < 2048; i += 32 * kEpiWarps) S.hist[i] = 0u;
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
     }
     const uint32_t acc_empty0 = map_shared_to_rank(smem_u32(&S.acc_empty[0]), 0);
@@ -303,11 +324,27 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       tc_fence_after();
       const int tmp = st / args.tiles_n, tn = st - tmp * args.tiles_n;
       const int tm = 2 * tmp + static_cast<int>(crank);  // past the last M tile: rows fail row_ok
-      epilogue_tile<BN, EPI, kEpiWarps>(args, S.b1, S.w2, S.part[buf], tmem + buf * BN, tm, tn,
-                                        r_in_tile, q, chalf);
+      epilogue_tile<BN, EPI, kEpiWarps>(args, S.b1, S.w2, S.part[buf], S.hist, tmem + buf * BN,
+                                        tm, tn, r_in_tile, q, chalf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + buf * 8);  // rank 0's acc_empty[buf]
+    }
+    if (EPI == EPI_GATE && args.sel_ws != nullptr) {
+      // this CTA's counts into the workspace; one thread stamps the header
+      // with the span, so that a select call on the same span skips its
+      // first pass
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+      for (int i = threadIdx.x - 64; i < 2048; i += 32 * kEpiWarps) {
+        const uint32_t c = S.hist[i];
+        if (c) atomicAdd(&args.sel_ws->gate_hist[i], c);
+      }
+      if (blockIdx.x == 0 && threadIdx.x == 64) {
+        args.sel_ws->hdr[0] = kSelectHistMagic;
+        args.sel_ws->hdr[1] = static_cast<uint32_t>(args.M);
+        args.sel_ws->hdr[2] = static_cast<uint32_t>(args.doc_b);
+        args.sel_ws->hdr[3] = static_cast<uint32_t>(args.doc_e);
+      }
     }
   }
 
@@ -352,8 +389,12 @@ cudaError_t launch_gemm_pair(const void* A, const void* B, const GemmArgs& a0,
 
 cudaError_t launch_gate_bf16(const void* X, int64_t N, int d, const void* W1, const float* b1,
                              int Hg, const float* w2, float b2, float* scores,
+                             SelectWorkspace* sel_ws, int64_t doc_b, int64_t doc_e,
                              cudaStream_t stream) {
   GemmArgs a{};
+  a.sel_ws = sel_ws;
+  a.doc_b = static_cast<int>(doc_b);
+  a.doc_e = static_cast<int>(doc_e);
   a.M = static_cast<int>(N);
   a.N = Hg;
   a.K = d;

@@ -212,11 +212,15 @@ const char* tg_last_error_message(void) { return tg::t_last_error; }
 
 tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d, const void* W1,
                         const float* b1, int32_t Hg, const float* w2, float b2, float* scores,
-                        tg_stream_t stream) {
+                        void* select_ws, int64_t doc_begin, int64_t doc_end, tg_stream_t stream) {
   TG_TRACE_CALL();
   TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "gate: bad dtype");
   TG_REQUIRE(N >= 0 && N < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "gate: N out of range");
   TG_REQUIRE(d > 0 && Hg > 0, TG_ERR_INVALID_ARG, "gate: d and Hg must be positive");
+  TG_REQUIRE(!select_ws || (0 <= doc_begin && doc_begin <= doc_end && doc_end <= N),
+             TG_ERR_INVALID_ARG, "gate: need 0 <= doc_begin <= doc_end <= N with a workspace");
+  TG_REQUIRE(!select_ws || (reinterpret_cast<uintptr_t>(select_ws) & 255u) == 0,
+             TG_ERR_INVALID_ARG, "gate: select workspace must be 256-byte aligned");
   if (N == 0) return TG_OK;
   TG_REQUIRE(X && W1 && w2 && scores, TG_ERR_INVALID_ARG, "gate: NULL pointer");
   TG_REQUIRE(aligned16(X) && aligned16(W1) && aligned16(w2) && aligned16(scores) &&
@@ -227,18 +231,29 @@ tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d, con
     TG_REQUIRE(d % 64 == 0, TG_ERR_UNSUPPORTED, "gate bf16: d %% 64 != 0 (d=%d)", d);
     TG_REQUIRE(Hg >= 16 && Hg <= 256 && Hg % 16 == 0, TG_ERR_UNSUPPORTED,
                "gate bf16: need 16 <= Hg <= 256, Hg %% 16 == 0 (Hg=%d)", Hg);
-    return from_cuda(tg::launch_gate_bf16(X, N, d, W1, b1, Hg, w2, b2, scores, st), "gate bf16");
+    return from_cuda(tg::launch_gate_bf16(X, N, d, W1, b1, Hg, w2, b2, scores,
+                                          static_cast<tg::SelectWorkspace*>(select_ws), doc_begin,
+                                          doc_end, st),
+                     "gate bf16");
   }
   TG_REQUIRE(d % 4 == 0, TG_ERR_UNSUPPORTED, "gate f32: d %% 4 != 0");
   TG_REQUIRE(Hg <= 1024, TG_ERR_UNSUPPORTED, "gate f32: Hg > 1024");
   TG_REQUIRE(static_cast<int64_t>(d) * 4 <= 200 * 1024, TG_ERR_UNSUPPORTED, "gate f32: d too big");
+  // the fp32 path does not fill the histogram: the select then runs its own
+  // first pass (the workspace header stays unstamped)
   return from_cuda(tg::launch_gate_f32(static_cast<const float*>(X), N, d,
                                        static_cast<const float*>(W1), b1, Hg, w2, b2, scores, st),
                    "gate f32");
 }
 
+size_t tg_select_workspace_bytes(int64_t N) {
+  (void)N;
+  return tg::kSelectWorkspaceBytes;
+}
+
 tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin, int64_t doc_end,
-                         int64_t K, int32_t* kept_idx, int64_t* M_out, tg_stream_t stream) {
+                         int64_t K, int32_t* kept_idx, int64_t* M_out, void* workspace,
+                         size_t workspace_bytes, tg_stream_t stream) {
   TG_TRACE_CALL();
   TG_REQUIRE(N >= 0 && N < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "select: N out of range");
   TG_REQUIRE(0 <= doc_begin && doc_begin <= doc_end && doc_end <= N, TG_ERR_INVALID_ARG,
@@ -251,7 +266,12 @@ tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin, int6
   TG_REQUIRE(scores && kept_idx, TG_ERR_INVALID_ARG, "select: NULL pointer");
   TG_REQUIRE(aligned16(scores) && aligned16(kept_idx), TG_ERR_INVALID_ARG,
              "select: pointers must be 16-byte aligned");
+  TG_REQUIRE(workspace != nullptr && workspace_bytes >= tg::kSelectWorkspaceBytes,
+             TG_ERR_INVALID_ARG, "select: need a workspace of tg_select_workspace_bytes() bytes");
+  TG_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, TG_ERR_INVALID_ARG,
+             "select: workspace must be 256-byte aligned");
   return from_cuda(tg::launch_select(scores, N, doc_begin, doc_end, K, kept_idx,
+                                     static_cast<tg::SelectWorkspace*>(workspace),
                                      reinterpret_cast<cudaStream_t>(stream)),
                    "select");
 }

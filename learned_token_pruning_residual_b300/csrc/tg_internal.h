@@ -59,9 +59,31 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// ---- the select workspace (caller-owned device memory, zeroed once before
+// its first use; every successful select call leaves it zeroed again)
+constexpr int kSelectMaxCtas = 256;
+constexpr uint32_t kSelectHistMagic = 0x74676831u;  // header stamp of a gate-filled histogram
+struct SelectWorkspace {
+  uint32_t hist[3][2048];           // radix histograms of the select's three passes
+  uint32_t gate_hist[2048];         // the first pass, counted by the gate epilogue
+  uint32_t cnt[kSelectMaxCtas][2];  // per-CTA (> T, == T) counts for the ordered compaction
+  uint32_t hdr[4];                  // {magic, N, doc_begin, doc_end} when the gate filled gate_hist
+  uint32_t bar_count, bar_gen;      // grid barrier: arrivals, generation
+};
+constexpr size_t kSelectWorkspaceBytes = 40960;
+static_assert(sizeof(SelectWorkspace) <= kSelectWorkspaceBytes, "select workspace");
+// Spans up to this many keys take the single-CTA select (all keys cached in
+// shared memory, no grid barrier); longer spans the multi-CTA one, whose
+// launch uses select_grid_size(D) CTAs.
+constexpr int64_t kSelectSmallMaxKeys = 45056;
+int select_grid_size(int64_t D);
+
 // ---- launchers (argument checking happens in the ABI layer)
+// sel_ws (nullable): accumulate the first radix histogram of the keys of
+// the scores in [doc_b, doc_e) into it for a following select call.
 cudaError_t launch_gate_bf16(const void* X, int64_t N, int d, const void* W1, const float* b1,
                              int Hg, const float* w2, float b2, float* scores,
+                             SelectWorkspace* sel_ws, int64_t doc_b, int64_t doc_e,
                              cudaStream_t stream);
 cudaError_t launch_gate_f32(const float* X, int64_t N, int d, const float* W1, const float* b1,
                             int Hg, const float* w2, float b2, float* scores,
@@ -71,7 +93,7 @@ cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int 
 cudaError_t launch_qkv_f32(const float* X, int64_t M, int d, const float* W, int ncols, float* Y,
                            cudaStream_t stream);
 cudaError_t launch_select(const float* scores, int64_t N, int64_t b, int64_t e, int64_t K,
-                          int32_t* idx, cudaStream_t stream);
+                          int32_t* idx, SelectWorkspace* ws, cudaStream_t stream);
 cudaError_t launch_gather(const void* X, int x_bf16, int64_t N, int d, const int32_t* idx,
                           int64_t M, void* Y, int y_bf16, const float* scores, float* logsig,
                           cudaStream_t stream);

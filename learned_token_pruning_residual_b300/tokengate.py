@@ -32,7 +32,7 @@ import torch
 
 __all__ = [
     "TokenGateError", "lib", "library_path", "TG_F32", "TG_BF16",
-    "tg_gate_score", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
+    "tg_gate_score", "tg_select_workspace_bytes", "new_select_workspace", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
     "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
     "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait", "gated_layer", "pruned_stack",
     "bias_backward", "EXPORTED_SYMBOLS",
@@ -51,8 +51,11 @@ _SIGNATURES = {
     "tg_status_string": [ctypes.c_int],
     "tg_abi_version": [],
     "tg_last_error_message": [],
-    "tg_gate_score": [_p, ctypes.c_int, _i64, _i32, _p, _p, _i32, _p, _f32, _p, _p],
-    "tg_select_topk": [_p, _i64, _i64, _i64, _i64, _p, ctypes.POINTER(_i64), _p],
+    "tg_gate_score": [_p, ctypes.c_int, _i64, _i32, _p, _p, _i32, _p, _f32, _p, _p, _i64, _i64,
+                      _p],
+    "tg_select_workspace_bytes": [_i64],
+    "tg_select_topk": [_p, _i64, _i64, _i64, _i64, _p, ctypes.POINTER(_i64), _p, ctypes.c_size_t,
+                       _p],
     "tg_gather_rows": [_p, ctypes.c_int, _i64, _i32, _p, _i64, _p, ctypes.c_int, _p, _p, _p],
     "tg_rmsnorm": [_p, ctypes.c_int, _i64, _i32, _p, _f32, _p, ctypes.c_int, _p],
     "tg_qkv_proj": [_p, ctypes.c_int, _i64, _i32, _p, _i32, _i32, _i32, _p, _p],
@@ -91,7 +94,7 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = args
             f.restype = ctypes.c_char_p if name in ("tg_status_string", "tg_last_error_message") \
-                else ctypes.c_int
+                else (ctypes.c_size_t if name == "tg_select_workspace_bytes" else ctypes.c_int)
         _lib = L
     return _lib
 
@@ -124,27 +127,60 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr()
 
 
-def tg_gate_score(X, W1, b1, w2, b2: float, out=None):
-    """Gate scores [N] fp32 of the residual rows X [N][d] (bf16 or fp32)."""
+def tg_gate_score(X, W1, b1, w2, b2: float, out=None, select_ws=None, doc_begin: int = 0,
+                  doc_end: int = 0):
+    """Gate scores [N] fp32 of the residual rows X [N][d] (bf16 or fp32).
+    With ``select_ws`` (a select workspace) the bf16 path also counts the
+    first radix pass of the selection over [doc_begin, doc_end) into it, for
+    the tg_select_topk that follows on the same workspace."""
     N, d = X.shape
     Hg = W1.shape[0]
     if out is None:
         out = torch.empty(N, dtype=torch.float32, device=X.device)
     _check(lib().tg_gate_score(_ptr(X), _dt(X), N, d, _ptr(W1), _ptr(b1), Hg, _ptr(w2),
-                               float(b2), _ptr(out), _stream()))
+                               float(b2), _ptr(out), _ptr(select_ws), int(doc_begin),
+                               int(doc_end), _stream()))
     return out
 
 
-def tg_select_topk(scores, doc_begin: int, doc_end: int, K: int, out=None):
+def tg_select_workspace_bytes(N: int = 0) -> int:
+    return int(lib().tg_select_workspace_bytes(int(N)))
+
+
+def new_select_workspace(device=None) -> torch.Tensor:
+    """A zeroed select workspace (uint8, tg_select_workspace_bytes() bytes)
+    on ``device``.  Every successful select leaves it zeroed again; use one
+    per stream."""
+    return torch.zeros(tg_select_workspace_bytes(), dtype=torch.uint8,
+                       device=device if device is not None else torch.cuda.current_device())
+
+
+_WORKSPACES: dict = {}
+
+
+def _default_workspace(device: torch.device) -> torch.Tensor:
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _WORKSPACES.get(key)
+    if ws is None:
+        ws = _WORKSPACES[key] = new_select_workspace(device)
+    return ws
+
+
+def tg_select_topk(scores, doc_begin: int, doc_end: int, K: int, out=None, workspace=None):
     """Ascending int32 indices of the kept tokens: all tokens outside
-    [doc_begin, doc_end) plus the K best-scoring document tokens."""
+    [doc_begin, doc_end) plus the K best-scoring document tokens.
+    ``workspace``: a select workspace (default: one kept per device and
+    stream by this module)."""
     N = scores.shape[0]
     M = N - (doc_end - doc_begin) + K
     if out is None:
         out = torch.empty(max(M, 0), dtype=torch.int32, device=scores.device)
+    if workspace is None:
+        workspace = _default_workspace(scores.device)
     m_out = _i64(0)
     _check(lib().tg_select_topk(_ptr(scores), N, doc_begin, doc_end, K, _ptr(out),
-                                ctypes.byref(m_out), _stream()))
+                                ctypes.byref(m_out), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream()))
     assert m_out.value == M
     return out
 
@@ -264,11 +300,17 @@ def tg_selftest_bounded_wait(timeout_us: int, report=None) -> None:
 def gated_layer(X, W1, b1, w2, b2, doc_begin, doc_end, K, Wqkv, Hq, Hkv, dh, gain, temperature,
                 bufs: dict | None = None):
     """One gated layer: score -> select -> gather -> QKV -> key-bias
-    attention, five library calls on the current stream.  ``bufs`` may hold
-    preallocated outputs (scores, idx, Xk, logsig, qkv, out)."""
+    attention, five library calls on the current stream.  The gate counts
+    the select's first radix pass into the select workspace.  ``bufs`` may
+    hold preallocated outputs (scores, idx, Xk, logsig, qkv, out) and the
+    workspace (select_ws)."""
     b = bufs or {}
-    s = tg_gate_score(X, W1, b1, w2, b2, out=b.get("scores"))
-    idx = tg_select_topk(s, doc_begin, doc_end, K, out=b.get("idx"))
+    ws = b.get("select_ws")
+    if ws is None:
+        ws = _default_workspace(X.device)
+    s = tg_gate_score(X, W1, b1, w2, b2, out=b.get("scores"), select_ws=ws, doc_begin=doc_begin,
+                      doc_end=doc_end)
+    idx = tg_select_topk(s, doc_begin, doc_end, K, out=b.get("idx"), workspace=ws)
     Xk, ls = tg_gather_rows(X, idx, s, out=b.get("Xk"), logsig_out=b.get("logsig"))
     qkv = tg_qkv_proj(Xk, Wqkv, Hq, Hkv, dh, out=b.get("qkv"))
     O = tg_keybias_attn(qkv, Hq, Hkv, dh, ls, gain, temperature, out=b.get("out"))

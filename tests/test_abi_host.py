@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.tg_abi_version() == 2
+    assert L.tg_abi_version() == 3
     names = [L.tg_status_string(i).decode() for i in range(7)]
     assert names == ["TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
                      "TG_ERR_NAN_SCORE", "TG_ERR_BAD_INDEX", "TG_ERR_TIMEOUT"]
@@ -49,36 +49,54 @@ def _m():
 
 def test_select_argument_errors_and_host_M(L):
     m = _m()
+    ws = ctypes.c_void_p(0x20000)
+    wsb = L.tg_select_workspace_bytes(0)
+    assert wsb == L.tg_select_workspace_bytes(1 << 30) == 40960   # independent of N
     # doc_end > N
-    assert L.tg_select_topk(None, 10, 2, 20, 1, None, ctypes.byref(m), None) == 1
+    assert L.tg_select_topk(None, 10, 2, 20, 1, None, ctypes.byref(m), ws, wsb, None) == 1
     assert b"doc_end" in L.tg_last_error_message()
     # K > D
-    assert L.tg_select_topk(None, 10, 2, 5, 4, None, ctypes.byref(m), None) == 1
+    assert L.tg_select_topk(None, 10, 2, 5, 4, None, ctypes.byref(m), ws, wsb, None) == 1
     # negative K
-    assert L.tg_select_topk(None, 10, 2, 5, -1, None, ctypes.byref(m), None) == 1
+    assert L.tg_select_topk(None, 10, 2, 5, -1, None, ctypes.byref(m), ws, wsb, None) == 1
     # N == 0 is valid and launches nothing; M is computed on the host
-    assert L.tg_select_topk(None, 0, 0, 0, 0, None, ctypes.byref(m), None) == 0
+    assert L.tg_select_topk(None, 0, 0, 0, 0, None, ctypes.byref(m), None, 0, None) == 0
     assert m.value == 0
     # nothing kept (M == 0) is valid and launches nothing
-    assert L.tg_select_topk(None, 3, 0, 3, 0, None, ctypes.byref(m), None) == 0
+    assert L.tg_select_topk(None, 3, 0, 3, 0, None, ctypes.byref(m), None, 0, None) == 0
     assert m.value == 0
     # NULL pointers with work to do
-    assert L.tg_select_topk(None, 10, 2, 5, 1, None, ctypes.byref(m), None) == 1
+    assert L.tg_select_topk(None, 10, 2, 5, 1, None, ctypes.byref(m), ws, wsb, None) == 1
     assert m.value == 8                                   # 10 - 3 + 1, reported before the check
     # misaligned pointer
     assert L.tg_select_topk(ctypes.c_void_p(0x1004), 10, 2, 5, 1, ctypes.c_void_p(0x2000),
-                            ctypes.byref(m), None) == 1
+                            ctypes.byref(m), ws, wsb, None) == 1
+    # the workspace: missing, too small, misaligned
+    p = ctypes.c_void_p(0x10000)
+    assert L.tg_select_topk(p, 10, 2, 5, 1, p, ctypes.byref(m), None, wsb, None) == 1
+    assert b"workspace" in L.tg_last_error_message()
+    assert L.tg_select_topk(p, 10, 2, 5, 1, p, ctypes.byref(m), ws, wsb - 1, None) == 1
+    assert L.tg_select_topk(p, 10, 2, 5, 1, p, ctypes.byref(m), ctypes.c_void_p(0x20010), wsb,
+                            None) == 1
 
 
 def test_gate_argument_errors(L):
     p = ctypes.c_void_p(0x10000)
-    assert L.tg_gate_score(p, 7, 10, 64, p, None, 16, p, 0.0, p, None) == 1          # dtype
-    assert L.tg_gate_score(p, 1, -1, 64, p, None, 16, p, 0.0, p, None) == 1          # N
-    assert L.tg_gate_score(p, 1, 10, 64, None, None, 16, p, 0.0, p, None) == 1       # NULL W1
-    assert L.tg_gate_score(p, 1, 10, 96, p, None, 16, p, 0.0, p, None) == 2          # d % 64
-    assert L.tg_gate_score(p, 1, 10, 64, p, None, 300, p, 0.0, p, None) == 2         # Hg > 256
-    assert L.tg_gate_score(p, 1, 10, 64, p, None, 24, p, 0.0, p, None) == 2          # Hg % 16
-    assert L.tg_gate_score(None, 1, 0, 64, None, None, 16, None, 0.0, None, None) == 0  # N == 0
+    g = lambda *a, ws=None, b=0, e=0: L.tg_gate_score(*a, ws, b, e, None)
+    assert g(p, 7, 10, 64, p, None, 16, p, 0.0, p) == 1          # dtype
+    assert g(p, 1, -1, 64, p, None, 16, p, 0.0, p) == 1          # N
+    assert g(p, 1, 10, 64, None, None, 16, p, 0.0, p) == 1       # NULL W1
+    assert g(p, 1, 10, 96, p, None, 16, p, 0.0, p) == 2          # d % 64
+    assert g(p, 1, 10, 64, p, None, 300, p, 0.0, p) == 2         # Hg > 256
+    assert g(p, 1, 10, 64, p, None, 24, p, 0.0, p) == 2          # Hg % 16
+    assert g(None, 1, 0, 64, None, None, 16, None, 0.0, None) == 0  # N == 0
+    # with a select workspace: the span must lie in [0, N], the workspace be aligned
+    ws = ctypes.c_void_p(0x20000)
+    assert g(p, 1, 10, 64, p, None, 16, p, 0.0, p, ws=ws, b=3, e=11) == 1
+    assert g(p, 1, 10, 64, p, None, 16, p, 0.0, p, ws=ws, b=5, e=4) == 1
+    assert g(p, 1, 10, 64, p, None, 16, p, 0.0, p, ws=ctypes.c_void_p(0x20040), b=0, e=8) == 1
+    # without a workspace the span is ignored
+    assert g(p, 1, 10, 96, p, None, 16, p, 0.0, p, b=5, e=4) == 2
 
 
 def test_gather_rmsnorm_qkv_attn_argument_errors(L):

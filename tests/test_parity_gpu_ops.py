@@ -100,6 +100,64 @@ def test_select_nan_in_span_sets_status():
     assert np.array_equal(got, O.select_topk(s3, 0, 3000, 100))
 
 
+def _ws_reset_words(ws):
+    """The workspace words that must be zero before a select call: the four
+    2048-word histograms, then (after 2 x 256 per-CTA count words) the
+    4-word header and the barrier's arrival counter."""
+    w = ws.view(torch.int32)
+    return torch.cat([w[:4 * 2048], w[4 * 2048 + 512:4 * 2048 + 512 + 5]])
+
+
+def test_select_leaves_workspace_zeroed():
+    ws = tg.new_select_workspace()
+    for N, b, e, K in [(131072, 0, 130816, 8176), (5000, 123, 4871, 4747), (5000, 0, 5000, 0),
+                       (300000, 1000, 299000, 29800)]:
+        s = TI.random_scores(N, seed=K + 1)
+        got = tg.tg_select_topk(to_dev(s), b, e, K, workspace=ws).cpu().numpy()
+        assert np.array_equal(got, O.select_topk(s, b, e, K))
+        assert int(_ws_reset_words(ws).count_nonzero()) == 0, (N, K)
+    assert _status() == 0
+
+
+@pytest.mark.parametrize("N,b,e,K", [(16384, 0, 16128, 1612), (131072, 0, 130816, 8176),
+                                     (20000, 300, 19000, 0), (20000, 300, 19000, 18700),
+                                     (4097, 1, 4096, 2000)])
+def test_gate_fills_first_select_pass(N, b, e, K):
+    """The gate epilogue counts the first radix pass into the select
+    workspace; the select on the same span uses it.  Bit-exact against the
+    oracle on the GPU's own scores, twice in a row on one workspace, and the
+    workspace is zero afterwards."""
+    d, Hg = 256, 64
+    rng = np.random.default_rng(N + K)
+    X = TI.f32_to_bf16_bits(rng.standard_normal((N, d)).astype(np.float32))
+    W1 = TI.f32_to_bf16_bits((rng.standard_normal((Hg, d)) / np.sqrt(d)).astype(np.float32))
+    w2 = (rng.standard_normal(Hg) / np.sqrt(Hg)).astype(np.float32)
+    Xd, W1d, w2d = to_dev(X), to_dev(W1), to_dev(w2)
+    ws = tg.new_select_workspace()
+    for _ in range(2):
+        sc = tg.tg_gate_score(Xd, W1d, None, w2d, 0.0, select_ws=ws, doc_begin=b, doc_end=e)
+        assert int(_ws_reset_words(ws).count_nonzero()) > 0 or e == b
+        idx = tg.tg_select_topk(sc, b, e, K, workspace=ws).cpu().numpy()
+        assert np.array_equal(idx, O.select_topk(sc.cpu().numpy(), b, e, K))
+        assert int(_ws_reset_words(ws).count_nonzero()) == 0
+    assert _status() == 0
+
+
+def test_gate_histogram_of_another_span_is_ignored():
+    N, d, Hg = 9000, 128, 32
+    rng = np.random.default_rng(4)
+    X = TI.f32_to_bf16_bits(rng.standard_normal((N, d)).astype(np.float32))
+    W1 = TI.f32_to_bf16_bits((rng.standard_normal((Hg, d)) / np.sqrt(d)).astype(np.float32))
+    w2 = (rng.standard_normal(Hg) / np.sqrt(Hg)).astype(np.float32)
+    ws = tg.new_select_workspace()
+    sc = tg.tg_gate_score(to_dev(X), to_dev(W1), None, to_dev(w2), 0.0, select_ws=ws,
+                          doc_begin=0, doc_end=8000)
+    idx = tg.tg_select_topk(sc, 100, 8500, 1234, workspace=ws).cpu().numpy()
+    assert np.array_equal(idx, O.select_topk(sc.cpu().numpy(), 100, 8500, 1234))
+    assert int(_ws_reset_words(ws).count_nonzero()) == 0
+    assert _status() == 0
+
+
 # ------------------------------------------------------------------ gather --
 @pytest.mark.parametrize("mode", ["bf16", "f32", "bf16_to_f32"])
 def test_gather_exact_and_logsig(mode):

@@ -191,7 +191,7 @@ def test_64k_stack20_teacher_forced_every_layer():
     x = torch.empty(M, w.d, dtype=torch.float32, device=Xd.device)
     _, ls = tg.tg_gather_rows(Xd, idx, s, out=x)
     x_ref, ls_ref = O.gather_rows(X, ref_idx, s32)
-    assert np.array_equal(f64(x), x_ref)
+    assert np.array_equal(f64(x), O.bf16_bits_to_f64(x_ref))
     np.testing.assert_allclose(f64(ls), ls_ref, rtol=2e-6, atol=1e-7)
     del Xd
     layers = _stack_layers(w, w.layers)
