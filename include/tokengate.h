@@ -151,6 +151,30 @@ tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin,
                          tg_stream_t stream);
 
 /*
+ * tg_select_topk without a workspace argument, for callers that cannot
+ * allocate device memory or hand the library a buffer: a host that owns all
+ * device memory and allows no allocation after start-up, a plug-in inside
+ * another framework's allocator, a C caller with no allocator at hand, or a
+ * latency-critical path (cudaMalloc can synchronise the device, cudaFree
+ * does).  The pages have no counterpart: this is a deployment variant of the
+ * select above, with the same arguments (minus the workspace), the same
+ * result and the same limits.  It allocates nothing: its scratch is a
+ * 40 KiB array compiled into the library, which every GPU that loads the
+ * library holds until the process exits.  A call whose scratch would not fit
+ * in the array returns TG_ERR_UNSUPPORTED (no N < 2^31 needs more today).
+ * The first call on each device looks up that device's array address
+ * (cudaGetSymbolAddress) while the device is current; make that first call
+ * outside any stream capture.  Each call clears the array on `stream`
+ * (cudaMemsetAsync) before its kernel.  All calls share the one array per
+ * device: calls that overlap on the GPU race and must not be made.  The
+ * gate's fused first-pass histogram (tg_gate_score's select_ws) is not used.
+ */
+tg_status tg_select_topk_noalloc(const float* scores, int64_t N,
+                                 int64_t doc_begin, int64_t doc_end, int64_t K,
+                                 int32_t* kept_idx, int64_t* M_out,
+                                 tg_stream_t stream);
+
+/*
  * Row gather ([IT] "TokenGate impara quali token mantenere": only the kept
  * tokens' representations go up; [DE] "Was ist token-gated Attention?":
  * their scores become the attention bias):

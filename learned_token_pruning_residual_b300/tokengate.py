@@ -19,6 +19,7 @@ Functions carry the C names:
     tg_bias_grad_reduce        dL/dlogsig, dL/dgain and dL/dscore from dL/db
     tg_get_device_status
     tg_selftest_bounded_wait   a wait that must give up (the failure path)
+    tg_select_topk_noalloc     the select without a workspace (scratch compiled in)
 
 plus three compositions of them, ``gated_layer``, ``pruned_stack`` and
 ``bias_backward``.
@@ -34,7 +35,8 @@ __all__ = [
     "TokenGateError", "lib", "library_path", "TG_F32", "TG_BF16",
     "tg_gate_score", "tg_select_workspace_bytes", "new_select_workspace", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
     "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
-    "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait", "gated_layer", "pruned_stack",
+    "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait",
+    "tg_select_topk_noalloc", "gated_layer", "pruned_stack",
     "bias_backward", "EXPORTED_SYMBOLS",
 ]
 
@@ -68,6 +70,7 @@ _SIGNATURES = {
     "tg_bias_grad_reduce": [_p, _i64, _i32, _p, _p, _p, _p, _p, _p],
     "tg_get_device_status": [_p],
     "tg_selftest_bounded_wait": [ctypes.c_uint32, _p, _p],
+    "tg_select_topk_noalloc": [_p, _i64, _i64, _i64, _i64, _p, ctypes.POINTER(_i64), _p],
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -181,6 +184,21 @@ def tg_select_topk(scores, doc_begin: int, doc_end: int, K: int, out=None, works
     _check(lib().tg_select_topk(_ptr(scores), N, doc_begin, doc_end, K, _ptr(out),
                                 ctypes.byref(m_out), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream()))
+    assert m_out.value == M
+    return out
+
+
+def tg_select_topk_noalloc(scores, doc_begin: int, doc_end: int, K: int, out=None):
+    """tg_select_topk for callers that cannot provide a workspace: the
+    library uses a scratch array compiled into it (one per device, shared by
+    all calls; calls must not overlap on the GPU)."""
+    N = scores.shape[0]
+    M = N - (doc_end - doc_begin) + K
+    if out is None:
+        out = torch.empty(max(M, 0), dtype=torch.int32, device=scores.device)
+    m_out = _i64(0)
+    _check(lib().tg_select_topk_noalloc(_ptr(scores), N, doc_begin, doc_end, K, _ptr(out),
+                                        ctypes.byref(m_out), _stream()))
     assert m_out.value == M
     return out
 
