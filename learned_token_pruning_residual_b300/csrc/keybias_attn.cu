@@ -537,9 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
-                             const float* logsig, const float* gain, float temperature, void* O,
-                             float* residual, float* lse, cudaStream_t stream) {
+cudaError_t launch_attn_bf16_2h(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
+                                const float* logsig, const float* gain, float temperature, void* O,
+                                float* residual, float* lse, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
   AttnArgs a{};
   a.M = static_cast<int>(M);

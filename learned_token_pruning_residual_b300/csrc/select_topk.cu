@@ -347,9 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Single-CTA select for spans that fit in shared memory (up to
-// kSelectSmallMaxKeys keys): no grid barrier, no global scratch beyond the
-// gate's histogram.  All keys are loaded once (16-byte loads, every thread's
+// Single-CTA select for short spans (up to kSelectSmallMaxKeys keys; its
+// time grows with the span, B300: 16128 keys 18 us, 32512 keys 26 us against
+// about 23 us for the multi-CTA select at any length): no grid barrier, no
+// global scratch beyond the gate's histogram.  All keys are loaded once (16-byte loads, every thread's
 // loads in flight together) into shared memory; the first pass's bin comes
 // from the gate's histogram when it is there; the other passes and the
 // ordered compaction (warp ballots over consecutive keys, a block scan of

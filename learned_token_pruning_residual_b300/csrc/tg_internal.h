@@ -75,7 +75,7 @@ static_assert(sizeof(SelectWorkspace) <= kSelectWorkspaceBytes, "select workspac
 // Spans up to this many keys take the single-CTA select (all keys cached in
 // shared memory, no grid barrier); longer spans the multi-CTA one, whose
 // launch uses select_grid_size(D) CTAs.
-constexpr int64_t kSelectSmallMaxKeys = 45056;
+constexpr int64_t kSelectSmallMaxKeys = 24576;
 int select_grid_size(int64_t D);
 
 // ---- launchers (argument checking happens in the ABI layer)
@@ -99,9 +99,19 @@ cudaError_t launch_gather(const void* X, int x_bf16, int64_t N, int d, const int
                           cudaStream_t stream);
 cudaError_t launch_rmsnorm(const void* X, int x_bf16, int64_t M, int d, const float* gamma,
                            float eps, void* Y, int y_bf16, cudaStream_t stream);
+// bf16 token-gated attention: dispatches to one of the two kernels below.
 cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
                              const float* logsig, const float* gain, float temperature, void* O,
                              float* residual, float* lse, cudaStream_t stream);
+// one CTA per (query block, pair of q heads of a kv head), heads ping-pong
+cudaError_t launch_attn_bf16_2h(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
+                                const float* logsig, const float* gain, float temperature, void* O,
+                                float* residual, float* lse, cudaStream_t stream);
+// persistent CTAs, one q head per work unit, key columns split over two
+// softmax warpgroups
+cudaError_t launch_attn_bf16_1h(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
+                                const float* logsig, const float* gain, float temperature, void* O,
+                                float* residual, float* lse, cudaStream_t stream);
 cudaError_t launch_attn_f32(const float* QKV, int64_t M, int Hq, int Hkv, int dh,
                             const float* logsig, const float* gain, float temperature, float* O,
                             float* residual, float* lse, cudaStream_t stream);
