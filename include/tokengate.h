@@ -221,6 +221,70 @@ tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d,
                       void* QKV, tg_stream_t stream);
 
 /*
+ * ---- A full decoder layer above the gate on the kept rows ([DE] "Wie hat
+ * TokenGate das Pruning von Tokens verstanden?": the layers above L process
+ * only the kept tokens; [IT] "TokenGate impara quali token mantenere": only
+ * their representations go up).  The layer's internals are the base model's
+ * (Qwen3): RMSNorm -> q|k|v -> per-head RMSNorm of q and k -> rotary
+ * embedding -> token-gated attention -> o-projection + residual -> RMSNorm
+ * -> SwiGLU MLP + residual.  The one pruning-specific choice: every kept row
+ * keeps its ORIGINAL prompt position for the rotary embedding (a kept row's
+ * result then equals the full prompt's at that row with the pruned keys
+ * masked).  bf16 operands, fp32 accumulation, an fp32 residual stream.
+ */
+
+/*
+ * Rotary table of the kept rows: for c < dh / 2,
+ *   table[m][c] = (cos, sin)(positions[m] * base^(-2c / dh)),
+ * [M][dh / 2][2] fp32, built once per prompt and shared by every layer.
+ * The angle is formed and reduced modulo 2 pi in fp64; its cosine and sine
+ * are taken in fp32.
+ *  positions  [M] int32, the rows' positions in the prompt (the kept
+ *             indices of tg_select_topk).
+ * Limits: dh even, 2..1024; base > 1.
+ */
+tg_status tg_rope_table(const int32_t* positions, int64_t M, int32_t dh, double base,
+                        float* table, tg_stream_t stream);
+
+/*
+ * QKV projection with Qwen3's per-head q/k RMSNorm and the rotary
+ * embedding, fused into the GEMM epilogue (the accumulator never leaves
+ * fp32 before the final bf16 store):
+ *   qkv = X Wqkv^T;  for each q head (gamma_q) and k head (gamma_k), row m:
+ *   y = x / sqrt(mean(x^2) + eps) * gamma;  then for c < dh / 2
+ *   (y_c, y_{c+dh/2}) <- (y_c cos - y_{c+dh/2} sin, y_{c+dh/2} cos + y_c sin)
+ *   with (cos, sin) = rope_table[m][c];  v heads unchanged.
+ *  X [M][d] bf16; Wqkv [(Hq + 2 Hkv) dh][d] bf16; QKV [M][(Hq + 2 Hkv) dh]
+ *  bf16 (layout of tg_qkv_proj); gamma_q, gamma_k [dh] fp32; rope_table as
+ *  tg_rope_table wrote it.
+ * Limits: dh == 128, d % 64 == 0, eps >= 0.
+ */
+tg_status tg_qkv_proj_qknorm_rope(const void* X, int64_t M, int32_t d, const void* Wqkv,
+                                  int32_t Hq, int32_t Hkv, int32_t dh, const float* gamma_q,
+                                  const float* gamma_k, float eps, const float* rope_table,
+                                  void* QKV, tg_stream_t stream);
+
+/*
+ * A projection added into the residual stream (the o-projection and the
+ * MLP's down-projection):  residual[m][n] += sum_k X[m][k] W[n][k].
+ *  X [M][K] bf16; W [N][K] bf16 (nn.Linear layout); residual [M][N] fp32,
+ *  updated in place.  Limits: K % 64 == 0, N % 32 == 0.
+ */
+tg_status tg_linear_residual(const void* X, int64_t M, int32_t K, const void* W, int32_t N,
+                             float* residual, tg_stream_t stream);
+
+/*
+ * The SwiGLU hidden layer:  Y = silu(X W_gate^T) * (X W_up^T),
+ * silu(z) = z / (1 + exp(-z)).  One GEMM: each CTA pair computes 128
+ * columns of both products, one CTA loading W_gate's rows, the other
+ * W_up's, and the epilogue multiplies them.
+ *  X [M][d] bf16; W_gate, W_up [F][d] bf16; Y [M][F] bf16.
+ * Limits: d % 64 == 0, F % 32 == 0.
+ */
+tg_status tg_swiglu(const void* X, int64_t M, int32_t d, const void* W_gate, const void* W_up,
+                    int32_t F, void* Y, tg_stream_t stream);
+
+/*
  * Token-gated causal attention over the kept rows ([DE] "Was ist
  * token-gated Attention?"; [TH] token-gated attention, per-head gain and
  * learnable temperature; [RU] "Механизм token-gated attention"):

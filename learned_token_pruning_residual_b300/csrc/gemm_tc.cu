@@ -27,7 +27,13 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-enum { EPI_STORE_BF16 = 0, EPI_GATE = 1 };
+enum {
+  EPI_STORE_BF16 = 0,  // C = acc, bf16
+  EPI_GATE = 1,        // s = w2 . GELU(acc + b1) + b2
+  EPI_QKNORM_ROPE = 2, // per-head RMSNorm of q and k, rotary embedding, bf16
+  EPI_RESID_ADD = 3,   // residual (fp32) += acc
+  EPI_SWIGLU = 4       // C = silu(acc[:, :BN/2]) * acc[:, BN/2:], bf16
+};
 
 // Epilogue warps: the gate's GELU.w2 head is arithmetic-heavy, so two warps
 // share each TMEM lane quadrant there, each taking half of the columns.
@@ -47,6 +53,14 @@ struct GemmArgs {
   float* scores;
   SelectWorkspace* sel_ws;  // EPI_GATE, nullable: first radix histogram of the span's keys
   int doc_b, doc_e;
+  // EPI_QKNORM_ROPE: heads of 128 columns; q heads [0, Hq), k heads
+  // [Hq, Hq + Hkv), then v; gamma_q / gamma_k [128]; rope [M][64] (cos, sin)
+  int Hq, Hkv;
+  const float* gamma_q;
+  const float* gamma_k;
+  float eps;
+  const float2* rope;
+  float* residual;  // EPI_RESID_ADD: [M][ldc] fp32
   uint32_t* status;
 };
 
@@ -104,6 +118,110 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, const float*
           for (int i = 0; i < 32 && col0 + i < args.N; ++i)
             d16[i] = static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
         }
+      }
+    }
+  } else if constexpr (EPI == EPI_QKNORM_ROPE) {
+    // the tile holds two heads of 128 columns; for a q or k head the row is
+    // normalised over its 128 columns (RMSNorm with gamma_q / gamma_k), then
+    // the pairs (c, c + 64) are rotated by the row's rotary angles
+#pragma unroll 1
+    for (int hh = 0; hh < BN / 128; ++hh) {
+      const int col0 = tn * BN + hh * 128;
+      const int hd = col0 / 128;
+      if (col0 >= args.N) break;
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(t_row + hh * 128 + c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c + i] = __uint_as_float(r[i]);
+      }
+      if (hd < args.Hq + args.Hkv) {
+        const float* gam = hd < args.Hq ? args.gamma_q : args.gamma_k;
+        float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          ss0 = fmaf(x[c], x[c], ss0);
+          ss1 = fmaf(x[c + 1], x[c + 1], ss1);
+        }
+        const float rstd = rsqrtf((ss0 + ss1) * (1.f / 128.f) + args.eps);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] *= rstd * __ldg(gam + c);
+        if (row_ok) {
+          const float4* cs = reinterpret_cast<const float4*>(args.rope + row * 64);
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float4 t = __ldg(cs + c / 2);  // (cos, sin) of pairs c and c + 1
+            const float a0 = x[c], b0 = x[c + 64], a1 = x[c + 1], b1 = x[c + 65];
+            x[c] = a0 * t.x - b0 * t.y;
+            x[c + 64] = b0 * t.x + a0 * t.y;
+            x[c + 1] = a1 * t.z - b1 * t.w;
+            x[c + 65] = b1 * t.z + a1 * t.w;
+          }
+        }
+      }
+      if (row_ok) {
+        uint4* d4 = reinterpret_cast<uint4*>(args.C + row * args.ldc + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          d4[i] = make_uint4(pack_bf16x2(x[8 * i + 0], x[8 * i + 1]),
+                             pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                             pack_bf16x2(x[8 * i + 4], x[8 * i + 5]),
+                             pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+      }
+    }
+  } else if constexpr (EPI == EPI_RESID_ADD) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(t_row + c0, r);
+      tmem_ld_wait();
+      const int col0 = tn * BN + c0;
+      if (row_ok && col0 < args.N) {
+        float4* dst = reinterpret_cast<float4*>(args.residual + row * args.ldc + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 v = dst[i];
+          v.x += __uint_as_float(r[4 * i + 0]);
+          v.y += __uint_as_float(r[4 * i + 1]);
+          v.z += __uint_as_float(r[4 * i + 2]);
+          v.w += __uint_as_float(r[4 * i + 3]);
+          dst[i] = v;
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    // columns [0, BN/2) of the tile are gate outputs, [BN/2, BN) the matching
+    // up outputs (the two CTAs of the pair load their halves of B from W_gate
+    // and W_up); silu(g) = g / (1 + 2^(-g log2 e))
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+      uint32_t gr[32], ur[32];
+      tmem_ld32(t_row + c0, gr);
+      tmem_ld32(t_row + BN / 2 + c0, ur);
+      tmem_ld_wait();
+      const int col0 = tn * (BN / 2) + c0;
+      if (row_ok && col0 < args.N / 2) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float y[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float gv = __uint_as_float(gr[2 * i + k]);
+            const float e = exp2_approx(-gv * 1.4426950408889634f);
+            float inv;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(1.f + e));
+            y[k] = gv * inv * __uint_as_float(ur[2 * i + k]);
+          }
+          pk[i] = pack_bf16x2(y[0], y[1]);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(args.C + row * args.ldc + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
     }
   } else {
@@ -172,7 +290,8 @@ struct PairSmem {
 template <int BN, int STAGES, int EPI>
 __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
   using Smem = PairSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -203,6 +322,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&S.tmem_base), kTmemCols);
@@ -236,8 +356,13 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           const uint32_t fb = map_shared_to_rank(smem_u32(&S.full[s]), 0);
           if (crank == 0) mbar_arrive_expect_tx(smem_u32(&S.full[s]), 2 * kStageBytes);
           tma_load_2d_pair(smem_u32(S.a[s]), &tmA, fb, kb * BK, tm * BM, pol_a);
-          tma_load_2d_pair(smem_u32(S.b[s]), &tmB, fb, kb * BK,
-                           tn * BN + static_cast<int>(crank) * (BN / 2), pol_b);
+          if (EPI == EPI_SWIGLU) {  // rank 0: W_gate rows, rank 1: W_up rows
+            tma_load_2d_pair(smem_u32(S.b[s]), crank ? &tmB2 : &tmB, fb, kb * BK,
+                             tn * (BN / 2), pol_b);
+          } else {
+            tma_load_2d_pair(smem_u32(S.b[s]), &tmB, fb, kb * BK,
+                             tn * BN + static_cast<int>(crank) * (BN / 2), pol_b);
+          }
           ++it;
         }
       }
@@ -359,19 +484,28 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 
 template <int BN, int STAGES, int EPI>
 cudaError_t launch_gemm_pair(const void* A, const void* B, const GemmArgs& a0,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const void* B2 = nullptr) {
   GemmArgs args = a0;
   args.tiles_n = (args.N + BN - 1) / BN;
   args.tiles_m = (args.M + BM - 1) / BM;
   args.num_super = ((args.tiles_m + 1) / 2) * args.tiles_n;
   args.status = device_status_word();
   if (args.tiles_m == 0 || args.tiles_n == 0) return cudaSuccess;
-  CUtensorMap tmA, tmB;
+  // B rows: N, or for the gate|up pair each of the two weights' N / 2 rows
+  const uint64_t b_rows = EPI == EPI_SWIGLU ? static_cast<uint64_t>(args.N / 2) : args.N;
+  CUtensorMap tmA, tmB, tmB2;
   if (!make_tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, args.M,
                     static_cast<uint64_t>(args.K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, args.N,
+      !make_tmap_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, b_rows,
                     static_cast<uint64_t>(args.K) * 2, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (EPI == EPI_SWIGLU) {
+    if (!make_tmap_2d(&tmB2, B2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, args.K, b_rows,
+                      static_cast<uint64_t>(args.K) * 2, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
+    tmB2 = tmB;  // unused
+  }
   auto kernel = gemm_bf16_pair_kernel<BN, STAGES, EPI>;
   const size_t smem = sizeof(PairSmem<BN, STAGES>) + 1024;
   cudaError_t err =
@@ -380,9 +514,33 @@ cudaError_t launch_gemm_pair(const void* A, const void* B, const GemmArgs& a0,
   const int max_pairs = sm_count() / 2;
   const int pairs = args.num_super < max_pairs ? args.num_super : max_pairs;
   err = launch_pdl(kernel, dim3(static_cast<unsigned>(2 * pairs)), dim3(gemm_threads(EPI)), smem,
-                   stream, 2u, tmA, tmB, args);
+                   stream, 2u, tmA, tmB, tmB2, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+// Rotary table of the kept rows: table[m][c] = (cos, sin)(pos[m] theta_c),
+// theta_c = base^(-2c / dh), c < dh / 2.  The angle is formed and reduced
+// modulo 2 pi in fp64 (a position near 131072 times theta_0 = 1 would lose
+// ~1e-2 rad in fp32); the reduced angle's cosine and sine are taken in fp32.
+__global__ void __launch_bounds__(256)
+    rope_table_kernel(const int32_t* __restrict__ pos, int64_t M, int half, double log2_base,
+                      float2* __restrict__ table) {
+  grid_dependency_wait();
+  allow_dependents_launch();
+  const int64_t n = M * half;
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = i / half;
+    const int c = static_cast<int>(i - m * half);
+    const double theta = exp2(-log2_base * (2.0 * c) / (2.0 * half));
+    const double a = static_cast<double>(__ldg(pos + m)) * theta;
+    const double r = a - kTwoPi * rint(a / kTwoPi);
+    float sn, cs;
+    sincosf(static_cast<float>(r), &sn, &cs);
+    table[i] = make_float2(cs, sn);
+  }
 }
 
 }  // namespace
@@ -415,6 +573,59 @@ cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int 
   a.C = static_cast<__nv_bfloat16*>(Y);
   a.ldc = ncols;
   return launch_gemm_pair<256, 6, EPI_STORE_BF16>(X, W, a, stream);
+}
+
+cudaError_t launch_qkv_qknorm_rope_bf16(const void* X, int64_t M, int d, const void* W, int Hq,
+                                       int Hkv, const float* gamma_q, const float* gamma_k,
+                                       float eps, const float2* rope, void* Y,
+                                       cudaStream_t stream) {
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = (Hq + 2 * Hkv) * 128;
+  a.K = d;
+  a.C = static_cast<__nv_bfloat16*>(Y);
+  a.ldc = a.N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.gamma_q = gamma_q;
+  a.gamma_k = gamma_k;
+  a.eps = eps;
+  a.rope = rope;
+  return launch_gemm_pair<256, 6, EPI_QKNORM_ROPE>(X, W, a, stream);
+}
+
+cudaError_t launch_linear_resid_bf16(const void* X, int64_t M, int K, const void* W, int N,
+                                     float* residual, cudaStream_t stream) {
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = N;
+  a.K = K;
+  a.residual = residual;
+  a.ldc = N;
+  return launch_gemm_pair<256, 6, EPI_RESID_ADD>(X, W, a, stream);
+}
+
+cudaError_t launch_swiglu_bf16(const void* X, int64_t M, int d, const void* Wg, const void* Wu,
+                               int F, void* Y, cudaStream_t stream) {
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = 2 * F;
+  a.K = d;
+  a.C = static_cast<__nv_bfloat16*>(Y);
+  a.ldc = F;
+  return launch_gemm_pair<256, 6, EPI_SWIGLU>(X, Wg, a, stream, Wu);
+}
+
+cudaError_t launch_rope_table(const int32_t* pos, int64_t M, int dh, double base, float2* table,
+                              cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  const int half = dh / 2;
+  const int64_t n = M * half;
+  const int64_t want = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  return launch_pdl(rope_table_kernel, dim3(grid), dim3(256), 0, stream, 1u, pos, M, half,
+                    log2(base), table);
 }
 
 }  // namespace tg

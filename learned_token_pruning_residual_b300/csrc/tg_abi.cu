@@ -341,6 +341,78 @@ tg_status tg_qkv_proj(const void* X, tg_dtype dtype, int64_t M, int32_t d, const
                    "qkv f32");
 }
 
+tg_status tg_rope_table(const int32_t* positions, int64_t M, int32_t dh, double base,
+                        float* table, tg_stream_t stream) {
+  TG_TRACE_CALL();
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31), TG_ERR_INVALID_ARG, "rope table: bad M");
+  TG_REQUIRE(dh > 0 && dh % 2 == 0 && dh <= 1024, TG_ERR_INVALID_ARG,
+             "rope table: dh must be even, 2..1024");
+  TG_REQUIRE(base > 1.0 && base < 1e300, TG_ERR_INVALID_ARG, "rope table: need base > 1");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(positions && table, TG_ERR_INVALID_ARG, "rope table: NULL pointer");
+  TG_REQUIRE(aligned16(positions) && aligned16(table), TG_ERR_INVALID_ARG,
+             "rope table: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_rope_table(positions, M, dh, base, reinterpret_cast<float2*>(table),
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                   "rope table");
+}
+
+tg_status tg_qkv_proj_qknorm_rope(const void* X, int64_t M, int32_t d, const void* Wqkv,
+                                  int32_t Hq, int32_t Hkv, int32_t dh, const float* gamma_q,
+                                  const float* gamma_k, float eps, const float* rope_table,
+                                  void* QKV, tg_stream_t stream) {
+  TG_TRACE_CALL();
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && d > 0 && Hq > 0 && Hkv > 0,
+             TG_ERR_INVALID_ARG, "qkv rope: bad sizes");
+  TG_REQUIRE(eps >= 0.f, TG_ERR_INVALID_ARG, "qkv rope: eps < 0");
+  TG_REQUIRE(dh == 128, TG_ERR_UNSUPPORTED, "qkv rope: dh must be 128");
+  TG_REQUIRE(d % 64 == 0, TG_ERR_UNSUPPORTED, "qkv rope: d %% 64 != 0");
+  TG_REQUIRE(static_cast<int64_t>(Hq + 2 * Hkv) * dh < (int64_t(1) << 20), TG_ERR_INVALID_ARG,
+             "qkv rope: too many columns");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(X && Wqkv && gamma_q && gamma_k && rope_table && QKV, TG_ERR_INVALID_ARG,
+             "qkv rope: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(Wqkv) && aligned16(QKV) && aligned16(rope_table),
+             TG_ERR_INVALID_ARG, "qkv rope: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_qkv_qknorm_rope_bf16(
+                       X, M, d, Wqkv, Hq, Hkv, gamma_q, gamma_k, eps,
+                       reinterpret_cast<const float2*>(rope_table), QKV,
+                       reinterpret_cast<cudaStream_t>(stream)),
+                   "qkv rope");
+}
+
+tg_status tg_linear_residual(const void* X, int64_t M, int32_t K, const void* W, int32_t N,
+                             float* residual, tg_stream_t stream) {
+  TG_TRACE_CALL();
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && K > 0 && N > 0, TG_ERR_INVALID_ARG,
+             "linear residual: bad sizes");
+  TG_REQUIRE(K % 64 == 0 && N % 32 == 0, TG_ERR_UNSUPPORTED,
+             "linear residual: need K %% 64 == 0 and N %% 32 == 0");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(X && W && residual, TG_ERR_INVALID_ARG, "linear residual: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(W) && aligned16(residual), TG_ERR_INVALID_ARG,
+             "linear residual: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_linear_resid_bf16(X, M, K, W, N, residual,
+                                                reinterpret_cast<cudaStream_t>(stream)),
+                   "linear residual");
+}
+
+tg_status tg_swiglu(const void* X, int64_t M, int32_t d, const void* W_gate, const void* W_up,
+                    int32_t F, void* Y, tg_stream_t stream) {
+  TG_TRACE_CALL();
+  TG_REQUIRE(M >= 0 && M < (int64_t(1) << 31) && d > 0 && F > 0, TG_ERR_INVALID_ARG,
+             "swiglu: bad sizes");
+  TG_REQUIRE(d % 64 == 0 && F % 32 == 0 && F <= (1 << 24), TG_ERR_UNSUPPORTED,
+             "swiglu: need d %% 64 == 0 and F %% 32 == 0");
+  if (M == 0) return TG_OK;
+  TG_REQUIRE(X && W_gate && W_up && Y, TG_ERR_INVALID_ARG, "swiglu: NULL pointer");
+  TG_REQUIRE(aligned16(X) && aligned16(W_gate) && aligned16(W_up) && aligned16(Y),
+             TG_ERR_INVALID_ARG, "swiglu: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_swiglu_bf16(X, M, d, W_gate, W_up, F, Y,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                   "swiglu");
+}
+
 tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq, int32_t Hkv,
                           int32_t dh, const float* logsig_kept, const float* gain,
                           float temperature, void* O, float* residual, tg_stream_t stream) {

@@ -90,6 +90,22 @@ cudaError_t launch_gate_f32(const float* X, int64_t N, int d, const float* W1, c
                             cudaStream_t stream);
 cudaError_t launch_qkv_bf16(const void* X, int64_t M, int d, const void* W, int ncols, void* Y,
                             cudaStream_t stream);
+// The layers of a full Qwen3 decoder layer on the kept rows (bf16, CTA-pair
+// tcgen05 GEMMs with fused epilogues):
+//  QKV with per-head q/k RMSNorm and the rotary embedding (dh = 128),
+cudaError_t launch_qkv_qknorm_rope_bf16(const void* X, int64_t M, int d, const void* W, int Hq,
+                                       int Hkv, const float* gamma_q, const float* gamma_k,
+                                       float eps, const float2* rope, void* Y,
+                                       cudaStream_t stream);
+//  residual (fp32 [M][N]) += X W^T,
+cudaError_t launch_linear_resid_bf16(const void* X, int64_t M, int K, const void* W, int N,
+                                     float* residual, cudaStream_t stream);
+//  Y = silu(X Wg^T) * (X Wu^T) ([M][F] bf16),
+cudaError_t launch_swiglu_bf16(const void* X, int64_t M, int d, const void* Wg, const void* Wu,
+                               int F, void* Y, cudaStream_t stream);
+//  and the rotary table of the kept rows ([M][dh / 2] (cos, sin)).
+cudaError_t launch_rope_table(const int32_t* pos, int64_t M, int dh, double base, float2* table,
+                              cudaStream_t stream);
 cudaError_t launch_qkv_f32(const float* X, int64_t M, int d, const float* W, int ncols, float* Y,
                            cudaStream_t stream);
 cudaError_t launch_select(const float* scores, int64_t N, int64_t b, int64_t e, int64_t K,

@@ -20,9 +20,13 @@ Functions carry the C names:
     tg_get_device_status
     tg_selftest_bounded_wait   a wait that must give up (the failure path)
     tg_select_topk_noalloc     the select without a workspace (scratch compiled in)
+    tg_rope_table              rotary (cos, sin) of the kept rows at their prompt positions
+    tg_qkv_proj_qknorm_rope    QKV projection + per-head q/k RMSNorm + rotary embedding
+    tg_linear_residual         residual += X W^T (o-projection, MLP down-projection)
+    tg_swiglu                  silu(X W_gate^T) * (X W_up^T)
 
-plus three compositions of them, ``gated_layer``, ``pruned_stack`` and
-``bias_backward``.
+plus compositions of them: ``gated_layer``, ``pruned_stack``, ``qwen3_layer``,
+``qwen3_pruned_stack`` and ``bias_backward``.
 """
 from __future__ import annotations
 
@@ -36,7 +40,8 @@ __all__ = [
     "tg_gate_score", "tg_select_workspace_bytes", "new_select_workspace", "tg_select_topk", "tg_gather_rows", "tg_rmsnorm", "tg_qkv_proj",
     "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
     "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait",
-    "tg_select_topk_noalloc", "gated_layer", "pruned_stack",
+    "tg_select_topk_noalloc", "tg_rope_table", "tg_qkv_proj_qknorm_rope", "tg_linear_residual",
+    "tg_swiglu", "qwen3_layer", "qwen3_pruned_stack", "gated_layer", "pruned_stack",
     "bias_backward", "EXPORTED_SYMBOLS",
 ]
 
@@ -71,6 +76,10 @@ _SIGNATURES = {
     "tg_get_device_status": [_p],
     "tg_selftest_bounded_wait": [ctypes.c_uint32, _p, _p],
     "tg_select_topk_noalloc": [_p, _i64, _i64, _i64, _i64, _p, ctypes.POINTER(_i64), _p],
+    "tg_rope_table": [_p, _i64, _i32, ctypes.c_double, _p, _p],
+    "tg_qkv_proj_qknorm_rope": [_p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _f32, _p, _p, _p],
+    "tg_linear_residual": [_p, _i64, _i32, _p, _i32, _p, _p],
+    "tg_swiglu": [_p, _i64, _i32, _p, _p, _i32, _p, _p],
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -313,6 +322,90 @@ def tg_selftest_bounded_wait(timeout_us: int, report=None) -> None:
     and of the abort-driven waiter.  Read the result with
     tg_get_device_status(raise_on_error=False): it returns TG_ERR_TIMEOUT."""
     _check(lib().tg_selftest_bounded_wait(int(timeout_us), _ptr(report), _stream()))
+
+
+def tg_rope_table(positions, dh: int, base: float, out=None):
+    """[M][dh/2][2] fp32 (cos, sin) of positions[m] * base^(-2c/dh)."""
+    M = positions.shape[0]
+    if out is None:
+        out = torch.empty(M, dh // 2, 2, dtype=torch.float32, device=positions.device)
+    _check(lib().tg_rope_table(_ptr(positions), M, dh, float(base), _ptr(out), _stream()))
+    return out
+
+
+def tg_qkv_proj_qknorm_rope(X, Wqkv, Hq: int, Hkv: int, dh: int, gamma_q, gamma_k, eps: float,
+                            rope_table, out=None):
+    M, d = X.shape
+    if out is None:
+        out = torch.empty(M, (Hq + 2 * Hkv) * dh, dtype=X.dtype, device=X.device)
+    _check(lib().tg_qkv_proj_qknorm_rope(_ptr(X), M, d, _ptr(Wqkv), Hq, Hkv, dh, _ptr(gamma_q),
+                                         _ptr(gamma_k), float(eps), _ptr(rope_table), _ptr(out),
+                                         _stream()))
+    return out
+
+
+def tg_linear_residual(X, W, residual):
+    """residual (fp32 [M][N], in place) += X W^T."""
+    M, K = X.shape
+    N = W.shape[0]
+    _check(lib().tg_linear_residual(_ptr(X), M, K, _ptr(W), N, _ptr(residual), _stream()))
+    return residual
+
+
+def tg_swiglu(X, W_gate, W_up, out=None):
+    M, d = X.shape
+    F = W_gate.shape[0]
+    if out is None:
+        out = torch.empty(M, F, dtype=X.dtype, device=X.device)
+    _check(lib().tg_swiglu(_ptr(X), M, d, _ptr(W_gate), _ptr(W_up), F, _ptr(out), _stream()))
+    return out
+
+
+def qwen3_layer(x, rope_table, L: dict, Hq: int, Hkv: int, dh: int, logsig, eps: float = 1e-6,
+                bufs: dict | None = None):
+    """One Qwen3 decoder layer on the kept rows, x (fp32 [M][d]) updated in
+    place: RMSNorm -> QKV + q/k RMSNorm + rotary embedding (rope_table of the
+    rows' prompt positions) -> token-gated attention -> x += o Wo^T ->
+    RMSNorm -> SwiGLU -> x += u Wd^T.  Seven library calls.  ``L`` holds
+    gamma_attn, Wqkv, gamma_q, gamma_k, gain, temperature, Wo, gamma_mlp, Wg,
+    Wu, Wd (bf16 weights, fp32 vectors); ``bufs`` may hold xn, qkv, o, hn, u."""
+    M, d = x.shape
+    b = bufs or {}
+    dev = x.device
+    bf = torch.bfloat16
+    F = L["Wg"].shape[0]
+    xn = b.get("xn") if b.get("xn") is not None else torch.empty(M, d, dtype=bf, device=dev)
+    qkv = b.get("qkv") if b.get("qkv") is not None else \
+        torch.empty(M, (Hq + 2 * Hkv) * dh, dtype=bf, device=dev)
+    o = b.get("o") if b.get("o") is not None else torch.empty(M, Hq * dh, dtype=bf, device=dev)
+    u = b.get("u") if b.get("u") is not None else torch.empty(M, F, dtype=bf, device=dev)
+    tg_rmsnorm(x, L["gamma_attn"], eps, out=xn)
+    tg_qkv_proj_qknorm_rope(xn, L["Wqkv"], Hq, Hkv, dh, L["gamma_q"], L["gamma_k"], eps,
+                            rope_table, out=qkv)
+    tg_keybias_attn(qkv, Hq, Hkv, dh, logsig, L["gain"], L["temperature"], out=o)
+    tg_linear_residual(o, L["Wo"], x)
+    tg_rmsnorm(x, L["gamma_mlp"], eps, out=xn)
+    tg_swiglu(xn, L["Wg"], L["Wu"], out=u)
+    tg_linear_residual(u, L["Wd"], x)
+    return x
+
+
+def qwen3_pruned_stack(x, positions, layers, Hq: int, Hkv: int, dh: int, logsig,
+                       rope_base: float = 1e6, eps: float = 1e-6, bufs: dict | None = None):
+    """The Qwen3 layers above the gate on the kept rows: the rotary table of
+    the rows' prompt positions is built once, then qwen3_layer per layer."""
+    table = tg_rope_table(positions, dh, rope_base)
+    b = dict(bufs or {})
+    M, d = x.shape
+    bf = torch.bfloat16
+    for key, shape in (("xn", (M, d)), ("qkv", (M, (Hq + 2 * Hkv) * dh)), ("o", (M, Hq * dh))):
+        if b.get(key) is None:
+            b[key] = torch.empty(*shape, dtype=bf, device=x.device)
+    if layers and b.get("u") is None:
+        b["u"] = torch.empty(M, layers[0]["Wg"].shape[0], dtype=bf, device=x.device)
+    for L in layers:
+        qwen3_layer(x, table, L, Hq, Hkv, dh, logsig, eps, bufs=b)
+    return x
 
 
 def gated_layer(X, W1, b1, w2, b2, doc_begin, doc_end, K, Wqkv, Hq, Hkv, dh, gain, temperature,

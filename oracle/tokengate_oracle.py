@@ -64,10 +64,10 @@ from scipy.special import expit as _expit
 __all__ = [
     "bf16_bits_to_f64", "f32_to_f64", "gelu_erf", "gate_score",
     "score_key", "select_topk", "select_topk_by_rank", "SelectNaNError",
-    "logsigmoid", "gather_rows", "rmsnorm", "qkv_proj", "split_qkv",
+    "logsigmoid", "gather_rows", "rmsnorm", "linear", "qkv_proj", "split_qkv",
     "keybias_attn", "gated_layer", "pruned_stack",
     "keybias_attn_lse", "attn_delta", "keybias_attn_bias_grad", "bias_grad_reduce",
-    "qk_rmsnorm", "rope", "swiglu_mlp", "qwen3_pruned_layer",
+    "qk_rmsnorm", "rope_angles", "rope", "swiglu_hidden", "swiglu_mlp", "qwen3_pruned_layer",
 ]
 
 
@@ -208,9 +208,14 @@ def rmsnorm(x, gamma, eps: float) -> np.ndarray:
     return x * _widen(gamma)[None, :] / np.sqrt(ms + float(eps))
 
 
+def linear(X, W) -> np.ndarray:
+    """X W^T with W [out][in] (nn.Linear layout, no bias)."""
+    return _widen(X) @ _widen(W).T
+
+
 def qkv_proj(X, Wqkv) -> np.ndarray:
     """QKV = X Wqkv^T with Wqkv [(Hq + 2 Hkv) dh][d] (nn.Linear layout)."""
-    return _widen(X) @ _widen(Wqkv).T
+    return linear(X, Wqkv)
 
 
 def split_qkv(QKV, Hq: int, Hkv: int, dh: int):
@@ -446,6 +451,15 @@ def qk_rmsnorm(QKV, Hq: int, Hkv: int, dh: int, gamma_q, gamma_k, eps: float) ->
     return Y
 
 
+def rope_angles(positions, dh: int, base: float):
+    """(cos, sin) of positions[m] * theta_c, theta_c = base^(-2c / dh),
+    c < dh / 2: float64 [M][dh / 2] each."""
+    h2 = dh // 2
+    theta = float(base) ** (-2.0 * np.arange(h2, dtype=np.float64) / dh)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
 def rope(QKV, Hq: int, Hkv: int, dh: int, positions, base: float) -> np.ndarray:
     """Rotary embedding of the q and k heads: with h2 = dh / 2 and
     theta_c = base^(-2c / dh) for c < h2, row m's pair (x_c, x_{c + h2}) of
@@ -457,9 +471,8 @@ def rope(QKV, Hq: int, Hkv: int, dh: int, positions, base: float) -> np.ndarray:
     Y = _widen(QKV).copy()
     M = Y.shape[0]
     h2 = dh // 2
-    theta = float(base) ** (-2.0 * np.arange(h2, dtype=np.float64) / dh)
-    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
-    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    cos, sin = rope_angles(positions, dh, base)
+    cos, sin = cos[:, None, :], sin[:, None, :]
     heads = Hq + Hkv
     blk = Y[:, :heads * dh].reshape(M, heads, dh)
     lo, hi = blk[:, :, :h2].copy(), blk[:, :, h2:].copy()
@@ -469,16 +482,21 @@ def rope(QKV, Hq: int, Hkv: int, dh: int, positions, base: float) -> np.ndarray:
     return Y
 
 
-def swiglu_mlp(x, Wg, Wu, Wd) -> np.ndarray:
-    """(silu(x Wg^T) * (x Wu^T)) Wd^T with silu(z) = z * sigmoid(z);
-    Wg, Wu [ffn][d], Wd [d][ffn] (nn.Linear layout)."""
+def swiglu_hidden(x, Wg, Wu) -> np.ndarray:
+    """silu(x Wg^T) * (x Wu^T) with silu(z) = z * sigmoid(z); Wg, Wu
+    [ffn][d] (nn.Linear layout).  float64 [M][ffn]."""
     x = _widen(x)
     g = x @ _widen(Wg).T
-    return (g * _expit(g) * (x @ _widen(Wu).T)) @ _widen(Wd).T
+    return g * _expit(g) * (x @ _widen(Wu).T)
+
+
+def swiglu_mlp(x, Wg, Wu, Wd) -> np.ndarray:
+    """The SwiGLU MLP: swiglu_hidden(x, Wg, Wu) Wd^T, Wd [d][ffn]."""
+    return swiglu_hidden(x, Wg, Wu) @ _widen(Wd).T
 
 
 def qwen3_pruned_layer(x, positions, L: dict, Hq: int, Hkv: int, dh: int, logsig_kept,
-                       eps: float = 1e-6) -> np.ndarray:
+                       eps: float = 1e-6, rows=None) -> np.ndarray:
     """One decoder layer on the kept rows, in Qwen3's order:
         a = RMSNorm(x; gamma_attn);  qkv = a Wqkv^T
         qkv = rope(qk_rmsnorm(qkv; gamma_q, gamma_k), positions; rope_base)
@@ -486,15 +504,16 @@ def qwen3_pruned_layer(x, positions, L: dict, Hq: int, Hkv: int, dh: int, logsig
         x = x + swiglu_mlp(RMSNorm(x; gamma_mlp); Wg, Wu, Wd)
     ``L`` holds those weights.  gamma_q None skips the q/k norm, rope_base
     None skips the rotary embedding, Wd None skips the MLP (the reductions
-    the pins use).  float64 [M][d]."""
+    the pins use).  ``rows`` (optional) restricts the output to those rows
+    (every row's keys still enter the attention).  float64 [M or len(rows)][d]."""
     x = _widen(x)
     qkv = qkv_proj(rmsnorm(x, L["gamma_attn"], eps), L["Wqkv"])
     if L.get("gamma_q") is not None:
         qkv = qk_rmsnorm(qkv, Hq, Hkv, dh, L["gamma_q"], L["gamma_k"], eps)
     if L.get("rope_base") is not None:
         qkv = rope(qkv, Hq, Hkv, dh, positions, L["rope_base"])
-    o = keybias_attn(qkv, Hq, Hkv, dh, logsig_kept, L["gain"], L["temperature"])
-    x = x + o @ _widen(L["Wo"]).T
+    o = keybias_attn(qkv, Hq, Hkv, dh, logsig_kept, L["gain"], L["temperature"], rows=rows)
+    x = (x if rows is None else x[np.asarray(rows)]) + linear(o, L["Wo"])
     if L.get("Wd") is not None:
         x = x + swiglu_mlp(rmsnorm(x, L["gamma_mlp"], eps), L["Wg"], L["Wu"], L["Wd"])
     return x

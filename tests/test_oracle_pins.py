@@ -698,6 +698,15 @@ def test_swiglu_matches_torch():
     ref = F.linear(F.silu(F.linear(t(x), t(Wg))) * F.linear(t(x), t(Wu)), t(Wd)).numpy()
     np.testing.assert_allclose(O.swiglu_mlp(x, Wg, Wu, Wd), ref, rtol=1e-12, atol=1e-12)
     assert not O.swiglu_mlp(x, Wg, Wu, np.zeros((d, ffn))).any()
+    hid = (F.silu(F.linear(t(x), t(Wg))) * F.linear(t(x), t(Wu))).numpy()
+    np.testing.assert_allclose(O.swiglu_hidden(x, Wg, Wu), hid, rtol=1e-12, atol=1e-12)
+    # silu(0) = 0 and silu(z) -> z for large z: the hidden layer of a zero
+    # gate weight is zero, of a huge positive gate it is (x Wg^T) (x Wu^T)
+    assert not O.swiglu_hidden(x, np.zeros((ffn, d)), Wu).any()
+    big = np.abs(Wg) * 0 + 1e3
+    xp = np.abs(x)
+    np.testing.assert_allclose(O.swiglu_hidden(xp, big, Wu), (xp @ big.T) * (xp @ Wu.T),
+                               rtol=1e-12)
 
 
 def _layer(rng, d, Hq, Hkv, dh, ffn):
@@ -747,3 +756,34 @@ def test_qwen3_layer_on_kept_rows_is_the_full_layer_with_pruned_keys_masked():
     # and the positions matter: compacted positions give a different result
     other = O.qwen3_pruned_layer(x[idx], np.arange(idx.size), L, Hq, Hkv, dh, ls[idx])
     assert np.abs(other - kept).max() > 1e-3
+
+
+def test_qwen3_layer_on_a_row_subset_equals_the_full_rows():
+    rng = np.random.default_rng(57)
+    Hq, Hkv, dh, M, ffn = 4, 2, 8, 37, 24
+    d = Hq * dh
+    x = rng.standard_normal((M, d))
+    ls = -rng.exponential(1.0, M)
+    L = _layer(rng, d, Hq, Hkv, dh, ffn)
+    pos = np.sort(rng.choice(1000, M, replace=False))
+    full = O.qwen3_pruned_layer(x, pos, L, Hq, Hkv, dh, ls)
+    rows = np.array([0, 5, 6, 20, 36])
+    np.testing.assert_allclose(O.qwen3_pruned_layer(x, pos, L, Hq, Hkv, dh, ls, rows=rows),
+                               full[rows], rtol=1e-12, atol=1e-12)
+
+
+def test_rope_angles_closed_forms():
+    cos, sin = O.rope_angles(np.array([0, 1, 131071]), 8, 1e6)
+    np.testing.assert_array_equal(cos[0], 1.0)
+    np.testing.assert_array_equal(sin[0], 0.0)
+    np.testing.assert_allclose(cos[1, 0], math.cos(1.0), rtol=1e-15)   # theta_0 = 1
+    np.testing.assert_allclose(sin[1, 1], math.sin(1e6 ** -0.25), rtol=1e-15)
+    np.testing.assert_allclose(cos ** 2 + sin ** 2, 1.0, rtol=1e-15)
+    np.testing.assert_allclose(sin[2, 0], math.sin(131071.0), rtol=1e-12)
+
+
+def test_linear_brute_force():
+    rng = np.random.default_rng(58)
+    X, W = rng.standard_normal((3, 5)), rng.standard_normal((4, 5))
+    ref = np.array([[sum(X[i, k] * W[j, k] for k in range(5)) for j in range(4)] for i in range(3)])
+    np.testing.assert_allclose(O.linear(X, W), ref, rtol=1e-13)

@@ -30,13 +30,15 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "kept_count", "f32_to_bf16_bits",
-    "residual", "gate_params", "qkv_weight", "attn_params", "rms_gamma",
+    "residual", "gate_params", "qkv_weight", "attn_params", "rms_gamma", "qwen3_layer_params",
     "random_scores", "random_qkv", "random_logsig", "random_dout", "adversarial_scores",
 ]
 
 # stream ids: one per tensor kind, so that draws never overlap
 _S_RESIDUAL, _S_W1, _S_B1, _S_W2, _S_B2, _S_WQKV, _S_GAIN, _S_GAMMA = range(8)
 _S_SCORES, _S_QKV, _S_LOGSIG, _S_ADV, _S_DOUT = 20, 21, 22, 23, 24
+# the other weights of a full (Qwen3-shaped) decoder layer
+_S_QK_GAMMA, _S_WO, _S_MLP_GAMMA, _S_WG, _S_WU, _S_WD = 30, 31, 32, 33, 34, 35
 
 
 @dataclass(frozen=True)
@@ -188,6 +190,30 @@ def attn_params(w: Workload, layer: int = 0) -> dict:
 
 def rms_gamma(w: Workload, layer: int = 0) -> np.ndarray:
     return _rng(w.seed, _S_GAMMA, layer).uniform(0.9, 1.1, size=w.d).astype(np.float32)
+
+
+def qwen3_layer_params(w: Workload, layer: int = 0, ffn: int = 6144) -> dict:
+    """All weights of one Qwen3-shaped decoder layer above the gate (the
+    pages' layers above L are the base model's layers; Qwen3-1.7B has an
+    MLP width of 6144 and a rotary base of 1e6):
+      gamma_attn, gamma_mlp [d] ~ U(0.9, 1.1); Wqkv as qkv_weight;
+      gamma_q, gamma_k [dh] ~ U(0.9, 1.1); gain, temperature as attn_params;
+      Wo [d][Hq dh] ~ N(0, 1/(Hq dh)); Wg, Wu [ffn][d] ~ N(0, 1/d);
+      Wd [d][ffn] ~ N(0, 1/ffn); matrices in the workload's dtype."""
+    qg = _rng(w.seed, _S_QK_GAMMA, layer)
+    return {
+        "gamma_attn": rms_gamma(w, layer), "Wqkv": qkv_weight(w, layer),
+        "gamma_q": qg.uniform(0.9, 1.1, size=w.dh).astype(np.float32),
+        "gamma_k": qg.uniform(0.9, 1.1, size=w.dh).astype(np.float32),
+        "rope_base": 1e6, **attn_params(w, layer),
+        "Wo": _normal(w.seed, _S_WO, layer, (w.d, w.Hq * w.dh), 1.0 / np.sqrt(w.Hq * w.dh),
+                      w.dtype),
+        "gamma_mlp": _rng(w.seed, _S_MLP_GAMMA, layer).uniform(0.9, 1.1, size=w.d)
+                       .astype(np.float32),
+        "Wg": _normal(w.seed, _S_WG, layer, (ffn, w.d), 1.0 / np.sqrt(w.d), w.dtype),
+        "Wu": _normal(w.seed, _S_WU, layer, (ffn, w.d), 1.0 / np.sqrt(w.d), w.dtype),
+        "Wd": _normal(w.seed, _S_WD, layer, (w.d, ffn), 1.0 / np.sqrt(ffn), w.dtype),
+    }
 
 
 def random_scores(n: int, seed: int, scale: float = 1.0) -> np.ndarray:
