@@ -666,15 +666,25 @@ def run_compare(args, w, K, rank, world, local_rank):
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(a).to(dev)
 
-    stack = w.layers > 1
+    qwen3 = args.decoder == "qwen3"
+    stack = w.layers > 1 or qwen3
     M = w.M(K)
     X_host = TI.residual(w)
     gp = TI.gate_params(w)
-    layers_h = [{"Wqkv": TI.qkv_weight(w, layer=i), "gamma": TI.rms_gamma(w, layer=i),
-                 **TI.attn_params(w, layer=i)} for i in range(w.layers)]
     W1, b1, w2 = to_dev(gp["W1"]), to_dev(gp["b1"]), to_dev(gp["w2"])
-    layers = [{"Wqkv": to_dev(L["Wqkv"]), "gamma": to_dev(L["gamma"]), "gain": to_dev(L["gain"]),
-               "temperature": L["temperature"]} for L in layers_h]
+    if qwen3:
+        # full Qwen3 decoder layers (q/k norm, rotary embedding at the prompt
+        # positions, o-projection, SwiGLU MLP); weights moved to the device one
+        # layer at a time
+        layers = []
+        for i in range(w.layers):
+            P = TI.qwen3_layer_params(w, layer=i)
+            layers.append({k: (to_dev(v) if isinstance(v, np.ndarray) else v) for k, v in P.items()})
+    else:
+        layers_h = [{"Wqkv": TI.qkv_weight(w, layer=i), "gamma": TI.rms_gamma(w, layer=i),
+                     **TI.attn_params(w, layer=i)} for i in range(w.layers)]
+        layers = [{"Wqkv": to_dev(L["Wqkv"]), "gamma": to_dev(L["gamma"]),
+                   "gain": to_dev(L["gain"]), "temperature": L["temperature"]} for L in layers_h]
     X = to_dev(X_host)
     bf, f32 = torch.bfloat16, torch.float32
 
@@ -705,7 +715,11 @@ def run_compare(args, w, K, rank, world, local_rank):
         s = tg.tg_gate_score(X, W1, b1, w2, gp["b2"], out=b["scores"], select_ws=b["ws"],
                              doc_begin=w.doc_begin, doc_end=w.doc_end)
         idx = tg.tg_select_topk(s, w.doc_begin, w.doc_end, K, out=b["idx"], workspace=b["ws"])
-        if stack:
+        if qwen3:
+            tg.tg_gather_rows(X, idx, s, out=b["x"], logsig_out=b["logsig"])
+            tg.qwen3_pruned_stack(b["x"], idx, layers, w.Hq, w.Hkv, w.dh, b["logsig"],
+                                  bufs={"xn": b["xn"], "qkv": b["qkv"]})
+        elif stack:
             tg.tg_gather_rows(X, idx, s, out=b["x"], logsig_out=b["logsig"])
             tg.pruned_stack(b["x"], layers, w.Hq, w.Hkv, w.dh, b["logsig"],
                             bufs={"xn": b["xn"], "qkv": b["qkv"]})
@@ -716,8 +730,14 @@ def run_compare(args, w, K, rank, world, local_rank):
             tg.tg_keybias_attn(b["qkv"], w.Hq, w.Hkv, w.dh, ls, L0["gain"], L0["temperature"],
                                out=b["out"])
 
+    positions_all = torch.arange(w.N, dtype=torch.int32, device=dev)
+
     def full(b):
-        if stack:
+        if qwen3:
+            tg.tg_gather_rows(X, None, out=b["x"])  # widen the residual to fp32
+            tg.qwen3_pruned_stack(b["x"], positions_all, layers, w.Hq, w.Hkv, w.dh, None,
+                                  bufs={"xn": b["xn"], "qkv": b["qkv"]})
+        elif stack:
             tg.tg_gather_rows(X, None, out=b["x"])  # widen the residual to fp32
             tg.pruned_stack(b["x"], layers, w.Hq, w.Hkv, w.dh, None,
                             bufs={"xn": b["xn"], "qkv": b["qkv"]})
@@ -750,14 +770,18 @@ def run_compare(args, w, K, rank, world, local_rank):
         return ms, peak
 
     weights = sum(t.numel() * t.element_size() for t in [X, W1, b1, w2] +
-                  [v for L in layers for v in (L["Wqkv"], L["gamma"], L["gain"])])
+                  [v for L in layers for v in L.values() if isinstance(v, torch.Tensor)])
     steps, warmup = max(1, args.steps), max(3, args.warmup)
     g_ms, g_peak = measure(gated, gated_bufs, steps, warmup)
     f_ms, f_peak = measure(full, full_bufs, max(1, min(steps, 5)), 1)
     attn_flops_full = 2.0 * w.N * w.N * w.dh * w.Hq * w.layers
     line = {
-        "metric": ("20-layer pruned-stack prefill tokens/s, gated vs full" if stack else
+        "metric": (f"{w.layers}-layer Qwen3 decoder prefill tokens/s, gated vs full" if qwen3 else
+                   "20-layer pruned-stack prefill tokens/s, gated vs full" if stack else
                    "one-layer prefill tokens/s, gated vs full-context attention"),
+        "decoder": ("full Qwen3 layers: RMSNorm, QKV + q/k RMSNorm + rotary embedding at the "
+                    "prompt positions, token-gated attention, o-projection, RMSNorm, SwiGLU MLP "
+                    "(width 6144)" if qwen3 else "x <- x + attn(qkv(RMSNorm(x)))"),
         "value": w.N / (g_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
         "warmup": warmup, "ms_per_step": g_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "mode": "compare",
@@ -926,6 +950,9 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clock-soak", action="store_true",
                     help="skip the one-second replay that samples clocks under load")
+    ap.add_argument("--decoder", default="attention", choices=["attention", "qwen3"],
+                    help="--mode compare: layers of the stack, attention only (the workload's "
+                         "definition) or full Qwen3 decoder layers")
     ap.add_argument("--mode", default="step", choices=["step", "compare", "backward"],
                     help="step: the timed gated-prefill step (default); compare: gated path vs "
                          "full prefill on the same kernels, with peak device memory; backward: "
