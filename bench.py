@@ -415,16 +415,28 @@ def run_gpu(args, w, K, rank, world, local_rank):
     nev = len(KERNELS) + 1
     graph, graph_inst, gev = None, None, None
     side = torch.cuda.Stream(dev)
+    plan_args = (W1, b1, w2, gp["b2"], w.doc_begin, w.doc_end, K, Wqkv, w.Hq, w.Hkv, w.dh, gain,
+                 t)
+
+    def make_plan(bufs):
+        """The library's CUDA graph of the five calls on one buffer set."""
+        return tg.GatedLayerPlan(bufs["X"], *plan_args,
+                                 bufs={"scores": bufs["s"], "select_ws": bufs["ws"],
+                                       "idx": bufs["idx"], "Xk": bufs["Xk"],
+                                       "logsig": bufs["ls"], "qkv": bufs["qkv"],
+                                       "out": bufs["out"]})
+
     if not args.no_graph:
-        # The step as one CUDA graph (timed by events around each replay),
-        # and a second copy with an event-record node before and after every
-        # call, replayed separately, for the per-kernel device times.  The
-        # record nodes serialise the kernels (their prologues can no longer
-        # overlap the previous kernel's tail), so they stay out of the
-        # timed step.
+        # The step is the library's plan (tg_gated_layer_plan_create: the five
+        # calls captured into one CUDA graph), timed by events around each
+        # launch.  A second copy with an event-record node before and after
+        # every call, captured here and replayed separately, gives the
+        # per-kernel device times; the record nodes serialise the kernels
+        # (their prologues can no longer overlap the previous kernel's
+        # tail), so they stay out of the timed step.
         run_calls(calls_direct)  # load modules / set attributes outside capture
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
+        graph = make_plan(A)
         graph_inst = torch.cuda.CUDAGraph()
         gev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
         for ev in gev:  # torch creates the event handle on its first record
@@ -439,8 +451,6 @@ def run_gpu(args, w, K, rank, world, local_rank):
                 raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
 
         calls_side = make_calls(A, side.cuda_stream)
-        with torch.cuda.graph(graph, stream=side):
-            run_calls(calls_side)
         with torch.cuda.graph(graph_inst, stream=side):
             run_calls(calls_side, gev, record_node)
 
@@ -448,7 +458,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
         if graph is None:
             run_calls(calls_direct)
         else:
-            graph.replay()
+            graph.launch(stream.cuda_stream)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -479,7 +489,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
             run_calls(calls_direct, evs[k], lambda ev: ev.record(stream))
         else:
             evs[k][0].record(stream)
-            graph.replay()
+            graph.launch(stream.cuda_stream)
             evs[k][1].record(stream)
     torch.cuda.synchronize()
     clocks = None
@@ -540,6 +550,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
     outs_pin = [(torch.empty(M, w.Hq * w.dh, dtype=bf).pin_memory(),
                  torch.empty(M, dtype=torch.int32).pin_memory()) for _ in sets]
     copy = torch.cuda.Stream(dev)
+    set_plans = [graph, make_plan(B)] if graph is not None else None
     set_calls = [make_calls(b, stream.cuda_stream) for b in sets]
     h2d_done = [torch.cuda.Event() for _ in sets]
     comp_done = [torch.cuda.Event() for _ in sets]
@@ -559,7 +570,10 @@ def run_gpu(args, w, K, rank, world, local_rank):
             b["X"].copy_(X_pin, non_blocking=True)
             h2d_done[j].record(copy)
         stream.wait_event(h2d_done[j])
-        run_calls(set_calls[j])
+        if set_plans is not None:
+            set_plans[j].launch(stream.cuda_stream)
+        else:
+            run_calls(set_calls[j])
         comp_done[j].record(stream)
         with torch.cuda.stream(copy):
             copy.wait_event(comp_done[j])
@@ -614,9 +628,10 @@ def run_gpu(args, w, K, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": workload_config(w, K, world),
-        "timing": ("one CUDA graph per step, timed by events around each replay; per-kernel "
-                   "times from a separately replayed copy with an event-record node around "
-                   "every call" if graph is not None else "direct C-ABI calls"),
+        "timing": ("one launch per step of the library's plan (the five calls as one CUDA "
+                   "graph, tg_gated_layer_plan_create), timed by events around each launch; "
+                   "per-kernel times from a separately replayed copy with an event-record node "
+                   "around every call" if graph is not None else "direct C-ABI calls"),
         "roofline": roofline,
         "pipeline": pipeline,
         "attn_tflops": attn["TFLOP/s"],

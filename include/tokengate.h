@@ -382,6 +382,52 @@ tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
                               tg_stream_t stream);
 
 /*
+ * ---- The gated layer as one CUDA graph ([DE] "Wie hat TokenGate das
+ * Pruning von Tokens verstanden?": score every token, keep the top K, run
+ * the layers above on the kept rows).  A plan captures the five calls of one
+ * gated layer on fixed buffers -- tg_gate_score (counting the select's first
+ * radix pass into the select workspace), tg_select_topk, tg_gather_rows,
+ * tg_qkv_proj, tg_keybias_attn -- into a CUDA graph once; tg_plan_launch
+ * replays it with one launch per prompt, so a new prompt is written into X
+ * and the graph runs again.  bf16 path only.
+ */
+typedef struct tg_gated_layer_desc {
+  const void* X;           /* [N][d] bf16 residual at the gate layer            */
+  int64_t N;
+  int32_t d;
+  const void* W1;          /* [Hg][d] bf16                                      */
+  const float* b1;         /* [Hg] or NULL                                      */
+  int32_t Hg;
+  const float* w2;         /* [Hg]                                              */
+  float b2;
+  int64_t doc_begin, doc_end, K;
+  const void* Wqkv;        /* [(Hq + 2 Hkv) dh][d] bf16                         */
+  int32_t Hq, Hkv, dh;
+  const float* gain;       /* [Hq]                                              */
+  float temperature;
+  /* outputs and scratch, all owned by the caller */
+  float* scores;           /* [N]                                               */
+  void* select_ws;         /* tg_select_workspace_bytes(N) bytes, zeroed once   */
+  size_t select_ws_bytes;
+  int32_t* kept_idx;       /* [M], M = N - (doc_end - doc_begin) + K            */
+  void* Xk;                /* [M][d] bf16                                       */
+  float* logsig_kept;      /* [M]                                               */
+  void* QKV;               /* [M][(Hq + 2 Hkv) dh] bf16                         */
+  void* O;                 /* [M][Hq dh] bf16                                   */
+} tg_gated_layer_desc;
+
+typedef struct tg_plan_s* tg_plan_t;
+
+/* Captures the gated layer described by *desc (every argument check of the
+ * five calls runs here, once) and instantiates the graph.  *plan receives a
+ * handle to release with tg_plan_destroy.  Uses the current device. */
+tg_status tg_gated_layer_plan_create(const tg_gated_layer_desc* desc, tg_plan_t* plan);
+/* Replays the plan's graph on `stream` (asynchronous). */
+tg_status tg_plan_launch(tg_plan_t plan, tg_stream_t stream);
+/* Releases the graph; plan must not be in use on the GPU. */
+tg_status tg_plan_destroy(tg_plan_t plan);
+
+/*
  * Synchronises `stream`, then returns and clears the sticky device status
  * of the current device: TG_OK, or the first of TG_ERR_NAN_SCORE,
  * TG_ERR_BAD_INDEX, TG_ERR_TIMEOUT that is set.  TG_ERR_CUDA if the

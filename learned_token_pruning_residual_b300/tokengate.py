@@ -24,6 +24,8 @@ Functions carry the C names:
     tg_qkv_proj_qknorm_rope    QKV projection + per-head q/k RMSNorm + rotary embedding
     tg_linear_residual         residual += X W^T (o-projection, MLP down-projection)
     tg_swiglu                  silu(X W_gate^T) * (X W_up^T)
+    tg_gated_layer_plan_create / tg_plan_launch / tg_plan_destroy
+                               the five calls of a gated layer as one CUDA graph
 
 plus compositions of them: ``gated_layer``, ``pruned_stack``, ``qwen3_layer``,
 ``qwen3_pruned_stack`` and ``bias_backward``.
@@ -41,7 +43,8 @@ __all__ = [
     "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
     "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait",
     "tg_select_topk_noalloc", "tg_rope_table", "tg_qkv_proj_qknorm_rope", "tg_linear_residual",
-    "tg_swiglu", "qwen3_layer", "qwen3_pruned_stack", "gated_layer", "pruned_stack",
+    "tg_swiglu", "GatedLayerPlan", "qwen3_layer", "qwen3_pruned_stack", "gated_layer",
+    "pruned_stack",
     "bias_backward", "EXPORTED_SYMBOLS",
 ]
 
@@ -80,6 +83,9 @@ _SIGNATURES = {
     "tg_qkv_proj_qknorm_rope": [_p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _f32, _p, _p, _p],
     "tg_linear_residual": [_p, _i64, _i32, _p, _i32, _p, _p],
     "tg_swiglu": [_p, _i64, _i32, _p, _p, _i32, _p, _p],
+    "tg_gated_layer_plan_create": [_p, ctypes.POINTER(_p)],
+    "tg_plan_launch": [_p, _p],
+    "tg_plan_destroy": [_p],
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -359,6 +365,65 @@ def tg_swiglu(X, W_gate, W_up, out=None):
         out = torch.empty(M, F, dtype=X.dtype, device=X.device)
     _check(lib().tg_swiglu(_ptr(X), M, d, _ptr(W_gate), _ptr(W_up), F, _ptr(out), _stream()))
     return out
+
+
+class _GatedLayerDesc(ctypes.Structure):
+    _fields_ = [("X", _p), ("N", _i64), ("d", _i32), ("W1", _p), ("b1", _p), ("Hg", _i32),
+                ("w2", _p), ("b2", _f32), ("doc_begin", _i64), ("doc_end", _i64), ("K", _i64),
+                ("Wqkv", _p), ("Hq", _i32), ("Hkv", _i32), ("dh", _i32), ("gain", _p),
+                ("temperature", _f32), ("scores", _p), ("select_ws", _p),
+                ("select_ws_bytes", ctypes.c_size_t), ("kept_idx", _p), ("Xk", _p),
+                ("logsig_kept", _p), ("QKV", _p), ("O", _p)]
+
+
+class GatedLayerPlan:
+    """The five calls of one gated layer on fixed device buffers, captured
+    once into a CUDA graph by the library (tg_gated_layer_plan_create);
+    launch() replays it on the current stream.  Write a new prompt into
+    ``X`` between launches.  ``bufs`` holds the outputs (scores, idx, Xk,
+    logsig, qkv, out) and the select workspace (select_ws); missing ones are
+    allocated here.  The tensors are kept alive with the plan."""
+
+    def __init__(self, X, W1, b1, w2, b2, doc_begin, doc_end, K, Wqkv, Hq, Hkv, dh, gain,
+                 temperature, bufs: dict | None = None):
+        N, d = X.shape
+        M = N - (doc_end - doc_begin) + K
+        dev = X.device
+        b = dict(bufs or {})
+        f32, bf = torch.float32, torch.bfloat16
+        b.setdefault("scores", torch.empty(N, dtype=f32, device=dev))
+        b.setdefault("select_ws", new_select_workspace(dev))
+        b.setdefault("idx", torch.empty(M, dtype=torch.int32, device=dev))
+        b.setdefault("Xk", torch.empty(M, d, dtype=bf, device=dev))
+        b.setdefault("logsig", torch.empty(M, dtype=f32, device=dev))
+        b.setdefault("qkv", torch.empty(M, (Hq + 2 * Hkv) * dh, dtype=bf, device=dev))
+        b.setdefault("out", torch.empty(M, Hq * dh, dtype=bf, device=dev))
+        self.bufs = b
+        self._keep = (X, W1, b1, w2, Wqkv, gain)
+        ws = b["select_ws"]
+        desc = _GatedLayerDesc(
+            _ptr(X), N, d, _ptr(W1), _ptr(b1), W1.shape[0], _ptr(w2), float(b2), doc_begin,
+            doc_end, K, _ptr(Wqkv), Hq, Hkv, dh, _ptr(gain), float(temperature), _ptr(b["scores"]),
+            _ptr(ws), ws.numel() * ws.element_size(), _ptr(b["idx"]), _ptr(b["Xk"]),
+            _ptr(b["logsig"]), _ptr(b["qkv"]), _ptr(b["out"]))
+        handle = _p()
+        _check(lib().tg_gated_layer_plan_create(ctypes.byref(desc), ctypes.byref(handle)))
+        self._handle = handle
+
+    def launch(self, stream: int | None = None):
+        _check(lib().tg_plan_launch(self._handle, _stream() if stream is None else stream))
+        return self.bufs
+
+    def close(self):
+        if self._handle is not None and self._handle.value:
+            lib().tg_plan_destroy(self._handle)
+        self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def qwen3_layer(x, rope_table, L: dict, Hq: int, Hkv: int, dh: int, logsig, eps: float = 1e-6,

@@ -179,3 +179,9 @@ def test_selftest_bounded_wait_argument_errors(L):
     assert L.tg_selftest_bounded_wait(1000001, None, None) == 1      # longer than 1 s
     assert b"timeout_us" in L.tg_last_error_message()
     assert L.tg_selftest_bounded_wait(100, ctypes.c_void_p(0x1004), None) == 1  # misaligned report
+
+
+def test_plan_argument_errors(L):
+    assert L.tg_gated_layer_plan_create(None, None) == 1
+    assert L.tg_plan_launch(None, None) == 1
+    assert L.tg_plan_destroy(None) == 0

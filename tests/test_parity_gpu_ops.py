@@ -343,3 +343,30 @@ def test_attn_tiny_f32(bias):
                              to_dev(g), 1.1)
     ref = O.keybias_attn(QKV, w.Hq, w.Hkv, w.dh, ls, g, 1.1)
     np.testing.assert_allclose(f64(got), ref, rtol=1e-4, atol=1e-5)
+
+
+# ------------------------------------------------------------- the plan --
+def test_gated_layer_plan_matches_the_calls():
+    """The library's CUDA graph of the five calls gives exactly the outputs
+    of the calls made one by one (the same kernels), launch after launch,
+    also after a new prompt is written into its input buffer."""
+    w = TI.Workload("plan_bf16_n4096", N=4096, doc_begin=64, doc_end=3900, d=2048, Hg=256, Hq=16,
+                    Hkv=8, dh=128, dtype="bf16", seed=21, K_fixed=700)
+    gp, Wqkv, ap = TI.gate_params(w, gate_biases=True), TI.qkv_weight(w), TI.attn_params(w)
+    X = to_dev(TI.residual(w))
+    args = (to_dev(gp["W1"]), to_dev(gp["b1"]), to_dev(gp["w2"]), gp["b2"], w.doc_begin,
+            w.doc_end, w.Ks()[0], to_dev(Wqkv), w.Hq, w.Hkv, w.dh, to_dev(ap["gain"]),
+            ap["temperature"])
+    plan = tg.GatedLayerPlan(X, *args)
+    for k in range(3):
+        if k == 2:  # a new prompt in the same buffer
+            X.copy_(to_dev(TI.f32_to_bf16_bits(np.random.default_rng(3).standard_normal(
+                (w.N, w.d)).astype(np.float32))))
+        got = plan.launch()
+        ref = tg.gated_layer(X, *args)
+        torch.cuda.synchronize()
+        for a, b in (("scores", "scores"), ("idx", "idx"), ("logsig", "logsig")):
+            assert torch.equal(got[a], ref[b]), a
+        assert torch.equal(got["out"].view(torch.int16), ref["O"].view(torch.int16))
+    plan.close()
+    assert _status() == 0
