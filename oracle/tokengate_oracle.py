@@ -68,6 +68,7 @@ __all__ = [
     "keybias_attn", "gated_layer", "pruned_stack",
     "keybias_attn_lse", "attn_delta", "keybias_attn_bias_grad", "bias_grad_reduce",
     "qk_rmsnorm", "rope_angles", "rope", "swiglu_hidden", "swiglu_mlp", "qwen3_pruned_layer",
+    "gated_delta_rule", "gated_delta_rule_chunked",
 ]
 
 
@@ -517,3 +518,71 @@ def qwen3_pruned_layer(x, positions, L: dict, Hq: int, Hkv: int, dh: int, logsig
     if L.get("Wd") is not None:
         x = x + swiglu_mlp(rmsnorm(x, L["gamma_mlp"], eps), L["Wg"], L["Wu"], L["Wd"])
     return x
+
+
+# --------------------------------------------------------------------------
+# Gated-DeltaNet layers of a hybrid model ([TH] "การใช้งานกับโมเดล
+# hybrid-attention"; [DE] "Wird es auf Hybrid-Attention-Modellen
+# funktionieren?"; [IT] "I modelli ibridi ampliano le possibilità di
+# selezione dei token": the gate can sit in a Gated-DeltaNet layer of a
+# hybrid model whose other layers are full attention, and the DeltaNet layers
+# above it are pruned too).  The pages give no formula; the layer's
+# recurrence is the published gated delta rule, per head, with a state
+# S in R^{dv x dk}:
+#     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+#     o_t = S_t q_t
+# alpha_t in (0, 1] a decay gate, beta_t in [0, 1] the write strength.  A
+# pruned DeltaNet layer runs this recurrence over the kept tokens only, in
+# their prompt order (a pruned token neither decays nor writes the state).
+# --------------------------------------------------------------------------
+def gated_delta_rule(q, k, v, alpha, beta, S0=None):
+    """The recurrence, token by token (the definition).
+    q, k [T][H][dk], v [T][H][dv], alpha, beta [T][H]; S0 [H][dv][dk] or
+    None (zeros).  Returns (o [T][H][dv], S_T [H][dv][dk]), float64."""
+    q, k, v = _widen(q), _widen(k), _widen(v)
+    a, b = np.asarray(alpha, np.float64), np.asarray(beta, np.float64)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    S = np.zeros((H, dv, dk)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((T, H, dv))
+    for t in range(T):
+        for h in range(H):
+            kt = k[t, h]
+            # S (I - beta k k^T) = S - beta (S k) k^T
+            S[h] = a[t, h] * (S[h] - b[t, h] * np.outer(S[h] @ kt, kt)) + b[t, h] * np.outer(v[t, h], kt)
+            o[t, h] = S[h] @ q[t, h]
+    return o, S
+
+
+def gated_delta_rule_chunked(q, k, v, alpha, beta, S0=None, chunk: int = 64):
+    """The same recurrence evaluated chunk by chunk.  Within a chunk that
+    starts from state S (before its first token), with g_i the cumulative
+    product of alpha up to token i of the chunk, the delta-rule errors
+    u_i = v_i - alpha_i S_{i-1} k_i satisfy the unit lower-triangular system
+        u_i + sum_{j<i} (g_i / g_j) beta_j (k_i . k_j) u_j = v_i - g_i S k_i,
+    and then
+        o_i = g_i S q_i + sum_{j<=i} (g_i / g_j) beta_j (k_j . q_i) u_j
+        S  <- g_C S + sum_j (g_C / g_j) beta_j u_j k_j^T.
+    Same arguments and results as gated_delta_rule (float64)."""
+    q, k, v = _widen(q), _widen(k), _widen(v)
+    a, b = np.asarray(alpha, np.float64), np.asarray(beta, np.float64)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    S = np.zeros((H, dv, dk)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((T, H, dv))
+    for c0 in range(0, T, chunk):
+        c1 = min(T, c0 + chunk)
+        for h in range(H):
+            K, Q, V = k[c0:c1, h], q[c0:c1, h], v[c0:c1, h]
+            bet = b[c0:c1, h]
+            lg = np.cumsum(np.log(a[c0:c1, h]))          # log g_i
+            G = np.exp(lg[:, None] - lg[None, :])          # g_i / g_j
+            n = c1 - c0
+            A = np.tril(G * (K @ K.T) * bet[None, :], -1)  # j < i
+            rhs = V - np.exp(lg)[:, None] * (K @ S[h].T)
+            U = np.linalg.solve(np.eye(n) + A, rhs)
+            P = np.tril(G * (Q @ K.T)) * bet[None, :]      # j <= i
+            o[c0:c1, h] = np.exp(lg)[:, None] * (Q @ S[h].T) + P @ U
+            wC = np.exp(lg[-1] - lg) * bet                 # (g_C / g_j) beta_j
+            S[h] = np.exp(lg[-1]) * S[h] + (U * wC[:, None]).T @ K
+    return o, S

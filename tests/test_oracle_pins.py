@@ -787,3 +787,73 @@ def test_linear_brute_force():
     X, W = rng.standard_normal((3, 5)), rng.standard_normal((4, 5))
     ref = np.array([[sum(X[i, k] * W[j, k] for k in range(5)) for j in range(4)] for i in range(3)])
     np.testing.assert_allclose(O.linear(X, W), ref, rtol=1e-13)
+
+
+
+# ---------------------------------------- Gated-DeltaNet layers (NEXT-4) ---
+def _gdn_inputs(T, H, dk, dv, seed, unit_keys=True):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit_keys:
+        k /= np.linalg.norm(k, axis=2, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    alpha = rng.uniform(0.8, 1.0, (T, H))
+    beta = rng.uniform(0.0, 1.0, (T, H))
+    return q, k, v, alpha, beta
+
+
+def test_gated_delta_rule_closed_forms():
+    T, H, dk, dv = 6, 2, 8, 5
+    q, k, v, alpha, beta = _gdn_inputs(T, H, dk, dv, seed=61)
+    # beta = 0: nothing is written, the output is zero
+    o, S = O.gated_delta_rule(q, k, v, alpha, np.zeros((T, H)))
+    assert not o.any() and not S.any()
+    # one token: S = beta v k^T, o = beta v (k . q)
+    o, S = O.gated_delta_rule(q[:1], k[:1], v[:1], alpha[:1], beta[:1])
+    np.testing.assert_allclose(S[0], beta[0, 0] * np.outer(v[0, 0], k[0, 0]), rtol=1e-14)
+    np.testing.assert_allclose(o[0, 0], beta[0, 0] * v[0, 0] * (k[0, 0] @ q[0, 0]), rtol=1e-13)
+    # alpha = beta = 1 with orthonormal keys: the delta rule is linear
+    # attention, S = sum_t v_t k_t^T
+    Qm, _ = np.linalg.qr(np.random.default_rng(62).standard_normal((dk, dk)))
+    ko = np.stack([Qm[:T].reshape(T, dk)] * H, axis=1)
+    o, S = O.gated_delta_rule(q, ko, v, np.ones((T, H)), np.ones((T, H)))
+    np.testing.assert_allclose(S[1], sum(np.outer(v[t, 1], ko[t, 1]) for t in range(T)),
+                               atol=1e-13)
+    # alpha = beta = 1 and the same unit key twice: the second write replaces
+    # the first (S k = v, the delta rule's fixed point)
+    kk = np.repeat(k[:1], 2, axis=0)
+    o, S = O.gated_delta_rule(q[:2], kk, v[:2], np.ones((2, H)), np.ones((2, H)))
+    np.testing.assert_allclose(S[0] @ k[0, 0], v[1, 0], atol=1e-13)
+    # decay only (beta = 0 after a first write from the zero state, which the
+    # first alpha does not touch): the state shrinks by the later alphas
+    b = np.zeros((T, H))
+    b[0] = 1.0
+    o, S = O.gated_delta_rule(q, k, v, alpha, b)
+    np.testing.assert_allclose(S[0], np.prod(alpha[1:, 0]) * np.outer(v[0, 0], k[0, 0]),
+                               rtol=1e-12)
+
+
+def test_gated_delta_rule_chunked_equals_recurrent():
+    for T, chunk in ((50, 16), (64, 64), (7, 4), (130, 64)):
+        q, k, v, alpha, beta = _gdn_inputs(T, 3, 16, 12, seed=T)
+        S0 = np.random.default_rng(T).standard_normal((3, 12, 16)) * 0.1
+        o1, S1 = O.gated_delta_rule(q, k, v, alpha, beta, S0)
+        o2, S2 = O.gated_delta_rule_chunked(q, k, v, alpha, beta, S0, chunk=chunk)
+        np.testing.assert_allclose(o2, o1, rtol=1e-10, atol=1e-11)
+        np.testing.assert_allclose(S2, S1, rtol=1e-10, atol=1e-11)
+
+
+def test_pruned_deltanet_equals_full_sequence_with_noop_tokens():
+    # running the layer on the kept tokens only equals running it on the full
+    # sequence with every pruned token a no-op (alpha = 1, beta = 0), at the
+    # kept tokens' outputs
+    T, H, dk, dv = 40, 2, 8, 6
+    q, k, v, alpha, beta = _gdn_inputs(T, H, dk, dv, seed=63)
+    idx = np.array([0, 2, 3, 9, 10, 11, 20, 31, 32, 39])
+    a2, b2 = np.ones((T, H)), np.zeros((T, H))
+    a2[idx], b2[idx] = alpha[idx], beta[idx]
+    o_full, S_full = O.gated_delta_rule(q, k, v, a2, b2)
+    o_kept, S_kept = O.gated_delta_rule(q[idx], k[idx], v[idx], alpha[idx], beta[idx])
+    np.testing.assert_allclose(o_kept, o_full[idx], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S_kept, S_full, rtol=1e-12, atol=1e-13)
