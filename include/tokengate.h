@@ -382,6 +382,36 @@ tg_status tg_bias_grad_reduce(const float* dbias, int64_t M, int32_t Hq,
                               tg_stream_t stream);
 
 /*
+ * ---- Gated-DeltaNet layers of a hybrid model ([TH] "การใช้งานกับโมเดล
+ * hybrid-attention"; [DE] "Wird es auf Hybrid-Attention-Modellen
+ * funktionieren?"; [IT] "I modelli ibridi ampliano le possibilità di
+ * selezione dei token": the gate can sit in a Gated-DeltaNet layer of a
+ * hybrid model, and the DeltaNet layers above it are pruned too).  The pages
+ * give no formula; the recurrence is the published gated delta rule, per
+ * head h with a state S in R^{dv x dk}:
+ *   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *   o_t = S_t q_t.
+ * A pruned layer calls it on the kept tokens only (rows in prompt order):
+ * a pruned token neither decays nor writes the state.
+ *
+ *  q, k  [T][H][dk] in `dtype` (the caller normalises k; bf16 or fp32).
+ *  v     [T][H][dv] in `dtype`.
+ *  alpha [T][H] fp32 in (0, 1];  beta [T][H] fp32 in [0, 1].
+ *  S0    [H][dv][dk] fp32 initial state, or NULL for zero.
+ *  o     [T][H][dv] output in `dtype`.
+ *  S_out [H][dv][dk] fp32 final state, or NULL.
+ *  workspace  device, tg_gated_delta_rule_workspace_bytes(T, H) bytes (no
+ *             zeroing needed; every call overwrites what it reads).
+ * Evaluated in chunks of 64 tokens, fp32 arithmetic throughout.
+ * Limits: dk == dv == 128.
+ */
+size_t tg_gated_delta_rule_workspace_bytes(int64_t T, int32_t H);
+tg_status tg_gated_delta_rule(const void* q, const void* k, const void* v, tg_dtype dtype,
+                              const float* alpha, const float* beta, int64_t T, int32_t H,
+                              int32_t dk, int32_t dv, const float* S0, void* o, float* S_out,
+                              void* workspace, size_t workspace_bytes, tg_stream_t stream);
+
+/*
  * ---- The gated layer as one CUDA graph ([DE] "Wie hat TokenGate das
  * Pruning von Tokens verstanden?": score every token, keep the top K, run
  * the layers above on the kept rows).  A plan captures the five calls of one

@@ -413,6 +413,35 @@ tg_status tg_swiglu(const void* X, int64_t M, int32_t d, const void* W_gate, con
                    "swiglu");
 }
 
+size_t tg_gated_delta_rule_workspace_bytes(int64_t T, int32_t H) {
+  if (T < 0 || H <= 0) return 0;
+  return tg::deltanet_workspace_bytes(T, H);
+}
+
+tg_status tg_gated_delta_rule(const void* q, const void* k, const void* v, tg_dtype dtype,
+                              const float* alpha, const float* beta, int64_t T, int32_t H,
+                              int32_t dk, int32_t dv, const float* S0, void* o, float* S_out,
+                              void* workspace, size_t workspace_bytes, tg_stream_t stream) {
+  TG_TRACE_CALL();
+  TG_REQUIRE(dtype == TG_F32 || dtype == TG_BF16, TG_ERR_INVALID_ARG, "delta rule: bad dtype");
+  TG_REQUIRE(T >= 0 && T < (int64_t(1) << 31) && H > 0 && H <= 4096, TG_ERR_INVALID_ARG,
+             "delta rule: bad sizes");
+  TG_REQUIRE(dk == 128 && dv == 128, TG_ERR_UNSUPPORTED, "delta rule: need dk == dv == 128");
+  TG_REQUIRE(T * H * 128 < (int64_t(1) << 40), TG_ERR_UNSUPPORTED, "delta rule: too large");
+  if (T == 0) return TG_OK;
+  TG_REQUIRE(q && k && v && alpha && beta && o && workspace, TG_ERR_INVALID_ARG,
+             "delta rule: NULL pointer");
+  TG_REQUIRE(workspace_bytes >= tg::deltanet_workspace_bytes(T, H), TG_ERR_INVALID_ARG,
+             "delta rule: workspace smaller than tg_gated_delta_rule_workspace_bytes(T, H)");
+  TG_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(alpha) &&
+                 aligned16(beta) && aligned16(o) && aligned16(workspace) &&
+                 (!S0 || aligned16(S0)) && (!S_out || aligned16(S_out)),
+             TG_ERR_INVALID_ARG, "delta rule: pointers must be 16-byte aligned");
+  return from_cuda(tg::launch_deltanet(q, k, v, dtype == TG_BF16, alpha, beta, T, H, S0, o, S_out,
+                                       workspace, reinterpret_cast<cudaStream_t>(stream)),
+                   "delta rule");
+}
+
 tg_status tg_keybias_attn(const void* QKV, tg_dtype dtype, int64_t M, int32_t Hq, int32_t Hkv,
                           int32_t dh, const float* logsig_kept, const float* gain,
                           float temperature, void* O, float* residual, tg_stream_t stream) {

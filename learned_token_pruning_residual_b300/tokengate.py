@@ -24,6 +24,7 @@ Functions carry the C names:
     tg_qkv_proj_qknorm_rope    QKV projection + per-head q/k RMSNorm + rotary embedding
     tg_linear_residual         residual += X W^T (o-projection, MLP down-projection)
     tg_swiglu                  silu(X W_gate^T) * (X W_up^T)
+    tg_gated_delta_rule        the gated delta rule of a Gated-DeltaNet layer, chunked
     tg_gated_layer_plan_create / tg_plan_launch / tg_plan_destroy
                                the five calls of a gated layer as one CUDA graph
 
@@ -43,7 +44,7 @@ __all__ = [
     "tg_keybias_attn", "tg_keybias_attn_lse", "tg_attn_bwd_delta", "tg_keybias_attn_bias_grad",
     "tg_bias_grad_reduce", "tg_get_device_status", "tg_selftest_bounded_wait",
     "tg_select_topk_noalloc", "tg_rope_table", "tg_qkv_proj_qknorm_rope", "tg_linear_residual",
-    "tg_swiglu", "GatedLayerPlan", "qwen3_layer", "qwen3_pruned_stack", "gated_layer",
+    "tg_swiglu", "tg_gated_delta_rule", "GatedLayerPlan", "qwen3_layer", "qwen3_pruned_stack", "gated_layer",
     "pruned_stack",
     "bias_backward", "EXPORTED_SYMBOLS",
 ]
@@ -83,6 +84,9 @@ _SIGNATURES = {
     "tg_qkv_proj_qknorm_rope": [_p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _f32, _p, _p, _p],
     "tg_linear_residual": [_p, _i64, _i32, _p, _i32, _p, _p],
     "tg_swiglu": [_p, _i64, _i32, _p, _p, _i32, _p, _p],
+    "tg_gated_delta_rule_workspace_bytes": [_i64, _i32],
+    "tg_gated_delta_rule": [_p, _p, _p, ctypes.c_int, _p, _p, _i64, _i32, _i32, _i32, _p, _p, _p,
+                            _p, ctypes.c_size_t, _p],
     "tg_gated_layer_plan_create": [_p, ctypes.POINTER(_p)],
     "tg_plan_launch": [_p, _p],
     "tg_plan_destroy": [_p],
@@ -112,7 +116,7 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = args
             f.restype = ctypes.c_char_p if name in ("tg_status_string", "tg_last_error_message") \
-                else (ctypes.c_size_t if name == "tg_select_workspace_bytes" else ctypes.c_int)
+                else (ctypes.c_size_t if name.endswith("_workspace_bytes") else ctypes.c_int)
         _lib = L
     return _lib
 
@@ -365,6 +369,23 @@ def tg_swiglu(X, W_gate, W_up, out=None):
         out = torch.empty(M, F, dtype=X.dtype, device=X.device)
     _check(lib().tg_swiglu(_ptr(X), M, d, _ptr(W_gate), _ptr(W_up), F, _ptr(out), _stream()))
     return out
+
+
+def tg_gated_delta_rule(q, k, v, alpha, beta, S0=None, out=None, S_out=None, workspace=None):
+    """o [T][H][dv] (q's dtype) of the gated delta rule over T tokens;
+    q, k [T][H][dk], v [T][H][dv], alpha, beta [T][H] fp32, S0 / S_out
+    [H][dv][dk] fp32 (optional).  Returns (o, S_out)."""
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    if out is None:
+        out = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
+    nb = int(lib().tg_gated_delta_rule_workspace_bytes(T, H))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().tg_gated_delta_rule(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(alpha), _ptr(beta), T,
+                                     H, dk, dv, _ptr(S0), _ptr(out), _ptr(S_out), _ptr(workspace),
+                                     workspace.numel(), _stream()))
+    return out, S_out
 
 
 class _GatedLayerDesc(ctypes.Structure):

@@ -32,6 +32,7 @@ __all__ = [
     "Workload", "WORKLOADS", "kept_count", "f32_to_bf16_bits",
     "residual", "gate_params", "qkv_weight", "attn_params", "rms_gamma", "qwen3_layer_params",
     "random_scores", "random_qkv", "random_logsig", "random_dout", "adversarial_scores",
+    "deltanet_inputs",
 ]
 
 # stream ids: one per tensor kind, so that draws never overlap
@@ -39,6 +40,7 @@ _S_RESIDUAL, _S_W1, _S_B1, _S_W2, _S_B2, _S_WQKV, _S_GAIN, _S_GAMMA = range(8)
 _S_SCORES, _S_QKV, _S_LOGSIG, _S_ADV, _S_DOUT = 20, 21, 22, 23, 24
 # the other weights of a full (Qwen3-shaped) decoder layer
 _S_QK_GAMMA, _S_WO, _S_MLP_GAMMA, _S_WG, _S_WU, _S_WD = 30, 31, 32, 33, 34, 35
+_S_DN = 40  # Gated-DeltaNet layer inputs
 
 
 @dataclass(frozen=True)
@@ -275,3 +277,21 @@ def adversarial_scores(kind: str, n: int, seed: int = 0) -> np.ndarray:
 
 ADVERSARIAL_KINDS = ("all_equal", "quantised", "signed_zero", "infinities", "denormal",
                      "same_top_bits", "descending", "ascending")
+
+
+def deltanet_inputs(T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "f32") -> dict:
+    """Inputs of a Gated-DeltaNet layer's recurrence over T tokens: q ~
+    N(0, 1/dk), k uniform on the unit sphere (a normal draw scaled to unit
+    length), v ~ N(0, 1), decay alpha ~ U(0.9, 1), write strength beta ~
+    U(0, 1); q, k, v as fp32 or bf16 bits ([T][H][d]), alpha and beta fp32
+    [T][H].  For bf16 the unit keys are rounded after scaling."""
+    g = _rng(seed, _S_DN)
+    q = g.standard_normal((T, H, dk), dtype=np.float32) * np.float32(1 / np.sqrt(dk))
+    k = g.standard_normal((T, H, dk), dtype=np.float32)
+    k /= np.linalg.norm(k, axis=2, keepdims=True)
+    v = g.standard_normal((T, H, dv), dtype=np.float32)
+    alpha = g.uniform(0.9, 1.0, (T, H)).astype(np.float32)
+    beta = g.uniform(0.0, 1.0, (T, H)).astype(np.float32)
+    if dtype == "bf16":
+        q, k, v = f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+    return {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta}
