@@ -38,6 +38,8 @@ import tg_inputs as TI  # noqa: E402
 
 METRIC = "gated-prefill tokens/s at 16k–128k; key-bias attn TFLOP/s and % of roofline"
 DEFAULT_WORKLOAD = "qwen3_1p7b_n128k_keep6p25"
+# the hybrid model's gated layer is reported on a 32k prompt; 10% kept
+DELTANET_WORKLOAD = "qwen3_1p7b_n32k_sweep"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNELS = ("gate_score", "select_topk", "gather_rows", "qkv_proj", "keybias_attn")
@@ -952,13 +954,136 @@ def run_backward(args, w, K, rank, world, local_rank):
 
 
 
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def deltanet_flops(T: int, H: int, dk: int, dv: int) -> int:
+    """The recurrence's own count: per token and head, S k, the rank-one
+    update of S and S q, each dk x dv multiply-adds."""
+    return 6 * T * H * dk * dv
+
+
+def run_deltanet(args, w, K, rank, world, local_rank):
+    """The gated delta rule (the recurrence of a hybrid model's Gated-DeltaNet
+    layers) over the M kept tokens of the workload's prompt, against the same
+    recurrence over all N tokens (full prefill of that layer).  Inputs are
+    seeded q, k, v of the DeltaNet head shape (bf16) and fp32 decay and write
+    strength; the kept tokens are a seeded sorted subset of M positions.  Each
+    timed step is one C-ABI call (two kernels), the L2 flushed between steps
+    outside the events."""
+    import torch
+
+    import learned_token_pruning_residual_b300 as tg
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    L = tg.lib()
+    M, N = w.M(K), w.N
+    H, dk, dv = TI.DELTANET_SHAPE["H"], TI.DELTANET_SHAPE["dk"], TI.DELTANET_SHAPE["dv"]
+    x = TI.deltanet_inputs(N, H, dk, dv, seed=w.seed, dtype="bf16")
+    idx = np.sort(np.random.default_rng(w.seed).choice(N, M, replace=False))
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    def bufs(rows):
+        b = {n: to_dev(x[n] if rows is None else x[n][rows]) for n in ("q", "k", "v", "alpha",
+                                                                      "beta")}
+        T = b["q"].shape[0]
+        b["o"] = torch.empty(T, H, dv, dtype=torch.bfloat16, device=dev)
+        nb = int(L.tg_gated_delta_rule_workspace_bytes(T, H))
+        b["ws"] = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
+        b["T"] = T
+        return b
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+
+    def call(b):
+        st = L.tg_gated_delta_rule(b["q"].data_ptr(), b["k"].data_ptr(), b["v"].data_ptr(), 1,
+                                   b["alpha"].data_ptr(), b["beta"].data_ptr(), b["T"], H, dk,
+                                   dv, None, b["o"].data_ptr(), None, b["ws"].data_ptr(),
+                                   b["ws"].numel(), sh)
+        if st != 0:
+            raise tg.TokenGateError(st, L.tg_last_error_message().decode())
+
+    def measure(b, n_steps, sampler=None):
+        for _ in range(warmup):
+            flush.zero_()
+            call(b)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_steps)]
+        if sampler:
+            sampler.active = True
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            call(b)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.active = False
+        return float(np.mean([a.elapsed_time(c) for a, c in evs]))
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    kept, full = bufs(idx), bufs(None)
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    ms_kept = measure(kept, steps, sampler)
+    clocks = sampler.stop()
+    ms_full = measure(full, max(1, min(steps, 20)))
+    if tg.tg_get_device_status(raise_on_error=False) != 0:
+        raise RuntimeError("device status set during the delta rule")
+    props = torch.cuda.get_device_properties(dev)
+    sm_max = clocks.get("sm_max_mhz") or 2032.0
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    fl = deltanet_flops(M, H, dk, dv)
+    ach = fl / ms_kept / 1e9
+    line = {
+        "metric": "Gated-DeltaNet layer over the kept tokens: prompt tokens/s",
+        "value": N / (ms_kept * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_kept, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "mode": "deltanet",
+        "config": {"workload": f"gated delta rule, {H} heads of dk = dv = {dk}, over the kept "
+                               f"tokens of {w.name}", "N": N, "K": K, "M": M, "heads": H,
+                   "dk": dk, "dv": dv, "inputs": "q, k, v bf16; alpha, beta fp32",
+                   "l2": "flushed between steps (256 MiB write), outside the timed events",
+                   "launch": "direct C-ABI call (chunk preparation + state scan)"},
+        "full": {"ms": ms_full, "tokens_per_s": N / (ms_full * 1e-3), "T": N},
+        "speedup": ms_full / ms_kept,
+        "roofline": {"kernel": "gated_delta_rule (both kernels)", "bound": "alu",
+                     "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                     "traffic": None, "algorithmic": fl,
+                     "peak_source": "derived: SMs x 128 FP32 lanes x 2 flops x max SM clock"},
+        "gpu_launches": 2 * steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(TI.WORKLOADS))
-    ap.add_argument("--budget", type=int, default=0, help="index into the workload's budgets")
+    ap.add_argument("--workload", default=None, choices=sorted(TI.WORKLOADS),
+                    help=f"default {DEFAULT_WORKLOAD}; {DELTANET_WORKLOAD} for --mode deltanet")
+    ap.add_argument("--budget", type=int, default=None,
+                    help="index into the workload's budgets (default 0; 1, i.e. 10%%, for "
+                         "--mode deltanet)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the five calls directly instead of replaying one CUDA graph")
@@ -968,12 +1093,18 @@ def main(argv=None) -> int:
     ap.add_argument("--decoder", default="attention", choices=["attention", "qwen3"],
                     help="--mode compare: layers of the stack, attention only (the workload's "
                          "definition) or full Qwen3 decoder layers")
-    ap.add_argument("--mode", default="step", choices=["step", "compare", "backward"],
+    ap.add_argument("--mode", default="step", choices=["step", "compare", "backward", "deltanet"],
                     help="step: the timed gated-prefill step (default); compare: gated path vs "
                          "full prefill on the same kernels, with peak device memory; backward: "
-                         "the gradient path from the attention bias to the scorer")
+                         "the gradient path from the attention bias to the scorer; deltanet: the "
+                         "gated delta rule over the kept tokens vs over the whole prompt")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
+    dn = args.mode == "deltanet"
+    if args.workload is None:
+        args.workload = DELTANET_WORKLOAD if dn else DEFAULT_WORKLOAD
+    if args.budget is None:
+        args.budget = 1 if dn and args.workload == DELTANET_WORKLOAD else 0
     w = TI.WORKLOADS[args.workload]
     K = w.Ks()[args.budget]
     if args.impl == "reference":
@@ -982,6 +1113,8 @@ def main(argv=None) -> int:
         return run_compare(args, w, K, rank, world, local_rank)
     if args.mode == "backward":
         return run_backward(args, w, K, rank, world, local_rank)
+    if args.mode == "deltanet":
+        return run_deltanet(args, w, K, rank, world, local_rank)
     return run_gpu(args, w, K, rank, world, local_rank)
 
 

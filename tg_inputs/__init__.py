@@ -33,6 +33,7 @@ __all__ = [
     "residual", "gate_params", "qkv_weight", "attn_params", "rms_gamma", "qwen3_layer_params",
     "random_scores", "random_qkv", "random_logsig", "random_dout", "adversarial_scores",
     "deltanet_inputs",
+    "DELTANET_SHAPE",
 ]
 
 # stream ids: one per tensor kind, so that draws never overlap
@@ -277,6 +278,11 @@ def adversarial_scores(kind: str, n: int, seed: int = 0) -> np.ndarray:
 
 ADVERSARIAL_KINDS = ("all_equal", "quantised", "signed_zero", "infinities", "denormal",
                      "same_top_bits", "descending", "ascending")
+
+
+# Head shape of a Gated-DeltaNet layer: the pages name the hybrid model but
+# give none of its sizes; 16 heads with dk = dv = 128 are taken.
+DELTANET_SHAPE = {"H": 16, "dk": 128, "dv": 128}
 
 
 def deltanet_inputs(T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "f32") -> dict:
