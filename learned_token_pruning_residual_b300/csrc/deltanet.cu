@@ -27,7 +27,10 @@
 //                           the chunks in order with its 16 x dk block of S
 //                           in shared memory and writes its 16 output
 //                           columns of every token.
-// fp32 arithmetic on CUDA cores throughout (inputs bf16 or fp32).
+// fp32 inputs and arithmetic on CUDA cores throughout; bf16 inputs take the
+// tensor-core kernels of deltanet_tc.cu.
+#include <algorithm>
+
 #include "tg_device.cuh"
 #include "tg_internal.h"
 
@@ -290,7 +293,8 @@ cudaError_t launch_deltanet_t(const void* q, const void* k, const void* v, const
 
 size_t deltanet_workspace_bytes(int64_t T_len, int H) {
   const int64_t n_chunks = (T_len + kC - 1) / kC;
-  return static_cast<size_t>(n_chunks) * H * sizeof(ChunkRec);
+  return std::max(static_cast<size_t>(n_chunks) * H * sizeof(ChunkRec),
+                  deltanet_tc_workspace_bytes(T_len, H));
 }
 
 cudaError_t launch_deltanet(const void* q, const void* k, const void* v, int bf16,
@@ -298,9 +302,8 @@ cudaError_t launch_deltanet(const void* q, const void* k, const void* v, int bf1
                             const float* S0, void* o, float* S_out, void* workspace,
                             cudaStream_t stream) {
   if (T_len == 0) return cudaSuccess;
-  if (bf16)
-    return launch_deltanet_t<__nv_bfloat16>(q, k, v, alpha, beta, T_len, H, S0, o, S_out,
-                                            workspace, stream);
+  if (bf16)  // the tensor-core kernels (deltanet_tc.cu)
+    return launch_deltanet_tc(q, k, v, alpha, beta, T_len, H, S0, o, S_out, workspace, stream);
   return launch_deltanet_t<float>(q, k, v, alpha, beta, T_len, H, S0, o, S_out, workspace, stream);
 }
 

@@ -106,8 +106,14 @@ cudaError_t launch_swiglu_bf16(const void* X, int64_t M, int d, const void* Wg, 
 //  and the rotary table of the kept rows ([M][dh / 2] (cos, sin)).
 cudaError_t launch_rope_table(const int32_t* pos, int64_t M, int dh, double base, float2* table,
                               cudaStream_t stream);
-// Gated delta rule (Gated-DeltaNet layers), dk = dv = 128, chunked.
+// Gated delta rule (Gated-DeltaNet layers), dk = dv = 128, chunked; fp32
+// inputs on CUDA cores (deltanet.cu), bf16 inputs on the tensor cores
+// (deltanet_tc.cu).  The workspace size covers both.
 size_t deltanet_workspace_bytes(int64_t T_len, int H);
+size_t deltanet_tc_workspace_bytes(int64_t T_len, int H);
+cudaError_t launch_deltanet_tc(const void* q, const void* k, const void* v, const float* alpha,
+                               const float* beta, int64_t T_len, int H, const float* S0, void* o,
+                               float* S_out, void* workspace, cudaStream_t stream);
 cudaError_t launch_deltanet(const void* q, const void* k, const void* v, int bf16,
                             const float* alpha, const float* beta, int64_t T_len, int H,
                             const float* S0, void* o, float* S_out, void* workspace,

@@ -26,6 +26,12 @@ def f64(t: torch.Tensor) -> np.ndarray:
 GATE_REL = 1e-4          # scores: |gpu - orc| <= 1e-4 * max(|orc|, rms(orc))
 ATTN_MAX_ABS = 2e-2      # attention: max |gpu - orc| over compared outputs
 ATTN_MEAN_ABS = 1e-2     #            mean |gpu - orc|
+# gated delta rule on the tensor cores (bf16 operands, fp32 state and sums):
+# per element |gpu - orc| <= 2^-5 (|orc| + rms(orc)), mean |gpu - orc| <= 2^-7
+# rms(orc); about twice / three times what a model of the kernels' bf16
+# rounding points reaches (tests/test_deltanet_rounding_model.py)
+DELTA_MAX_REL = 2.0 ** -5
+DELTA_MEAN_REL = 2.0 ** -7
 
 
 def assert_gate_close(got, ref):
@@ -69,3 +75,14 @@ def assert_attn_close(got, ref):
     mx, mean = float(err.max()), float(err.mean())
     assert mx <= ATTN_MAX_ABS and mean <= ATTN_MEAN_ABS, f"max {mx:.3e} mean {mean:.3e}"
     return mx, mean
+
+
+def assert_delta_close(got, ref, what=""):
+    """The delta rule's bf16 tolerance; returns (max, mean) error over rms."""
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    err = np.abs(got - ref)
+    bad = err > DELTA_MAX_REL * (np.abs(ref) + rms)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} off, worst {float(err.max()):.3e} "
+                           f"(rms {rms:.3e})")
+    assert float(err.mean()) <= DELTA_MEAN_REL * rms, (what, float(err.mean()), rms)
+    return float(err.max()) / rms, float(err.mean()) / rms
