@@ -44,34 +44,47 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNELS = ("gate_score", "select_topk", "gather_rows", "qkv_proj", "keybias_attn")
 PIPELINE = ("gate_score", "select_topk", "gather_rows")  # the HBM-bound front of the step
-KERNEL_SOURCES = {"gate_score": "gemm_tc.cu", "select_topk": "select_topk.cu",
-                  "gather_rows": "rows.cu", "qkv_proj": "gemm_tc.cu",
-                  "keybias_attn": "keybias_attn.cu", "keybias_bias_grad": "attn_bwd.cu"}
+# the sources each kernel's code comes from (the attention dispatcher and
+# its short-sequence kernel live in keybias_attn_1h.cu)
+KERNEL_SOURCES = {"gate_score": ("gemm_tc.cu",), "select_topk": ("select_topk.cu",),
+                  "gather_rows": ("rows.cu",), "qkv_proj": ("gemm_tc.cu",),
+                  "keybias_attn": ("keybias_attn.cu", "keybias_attn_1h.cu"),
+                  "keybias_bias_grad": ("attn_bwd.cu",),
+                  "gated_delta_rule": ("deltanet.cu", "deltanet_tc.cu")}
 # DRAM bytes per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by workload/kernel, with the sha256 (first 16
 # hex) of the kernel's source at capture time; a stale hash reports null.
 NCU_TRAFFIC: dict[str, dict] = {
-    # Qwen3-1.7B shapes, N = 16384, 10% of the document kept
-    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15383552 + 768,
-                                            "source_sha": "9cd3022e6e5e9867"},
-    "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68187904 + 627456,
-                                          "source_sha": "25e1c47fd2f58bc2"},
-    "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24447744 + 512,
-                                        "source_sha": "25e1c47fd2f58bc2"},
-    "qwen3_1p7b_n16k_keep10/gather_rows": {"bytes_per_launch": 7728384,
+    # Qwen3-1.7B shapes, N = 16384, 10% of the document kept (M = 1868)
+    "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68191232 + 3328,
+                                          "source_sha": "0f25d4a8caaef008"},
+    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 103424,
+                                           "source_sha": "eff82ff787cf8a1d"},
+    "qwen3_1p7b_n16k_keep10/gather_rows": {"bytes_per_launch": 7729152,
                                            "source_sha": "27ffa82b44661223"},
-    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 92672,
-                                           "source_sha": "eab745ed225e14e2"},
-    # N = 131072, 6.25% of the document kept
-    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69858560 + 6637312,
-                                               "source_sha": "9cd3022e6e5e9867"},
-    "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537969920 + 3190016,
-                                             "source_sha": "25e1c47fd2f58bc2"},
-    "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51378432 + 24764416,
-                                           "source_sha": "25e1c47fd2f58bc2"},
+    "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24454656,
+                                        "source_sha": "0f25d4a8caaef008"},
+    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15368704,
+                                            "source_sha": "6290768b50105383"},
+    # N = 131072, 6.25% of the document kept (M = 8432)
+    "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537969664 + 328960,
+                                             "source_sha": "0f25d4a8caaef008"},
+    "qwen3_1p7b_n128k_keep6p25/select_topk": {"bytes_per_launch": 576512,
+                                              "source_sha": "eff82ff787cf8a1d"},
+    "qwen3_1p7b_n128k_keep6p25/gather_rows": {"bytes_per_launch": 35033344 + 46848,
+                                              "source_sha": "27ffa82b44661223"},
+    "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51425536 + 20341760,
+                                           "source_sha": "0f25d4a8caaef008"},
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69795072 + 3588352,
+                                               "source_sha": "6290768b50105383"},
     # the backward's bias-gradient kernel at M = 8432
     "qwen3_1p7b_n128k_keep6p25/keybias_bias_grad": {"bytes_per_launch": 137630464 + 3417344,
                                                     "source_sha": "3d91e7a27c9845f8"},
+    # the delta rule over the 3507 kept tokens of the 32k prompt (10% budget),
+    # both kernels of one call: chunk preparation + state scan
+    "qwen3_1p7b_n32k_sweep/gated_delta_rule": {
+        "bytes_per_launch": (29939456 + 6322688) + (72099328 + 3732480),
+        "source_sha": "4c12a2907c700e2b"},
 }
 
 
@@ -104,10 +117,14 @@ def load_peaks() -> tuple[dict, str]:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash(fname: str) -> str:
-    path = os.path.join(ROOT, "learned_token_pruning_residual_b300", "csrc", fname)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(fnames) -> str:
+    """sha256 (first 16 hex) of the named csrc files, concatenated in order."""
+    h = hashlib.sha256()
+    for fname in ([fnames] if isinstance(fnames, str) else fnames):
+        with open(os.path.join(ROOT, "learned_token_pruning_residual_b300", "csrc", fname),
+                  "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str, kernel: str):
@@ -954,13 +971,19 @@ def run_backward(args, w, K, rank, world, local_rank):
 
 
 
-FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
+DN_CHUNK = 64  # tokens per chunk of the chunked delta rule
 
 
-def deltanet_flops(T: int, H: int, dk: int, dv: int) -> int:
-    """The recurrence's own count: per token and head, S k, the rank-one
-    update of S and S q, each dk x dv multiply-adds."""
-    return 6 * T * H * dk * dv
+def deltanet_flops(T: int, H: int, dk: int, dv: int) -> dict:
+    """Products of the chunked form per chunk of C tokens and head: K K^T and
+    Q K^T (2 C^2 dk each), W = T diag(g) K (2 C^2 dk), U^T = V^T T^T (2 C^2 dv),
+    S W^T, S (diag(g) Q)^T and the update U^T K' (2 C dk dv each), and
+    U^T P^T (2 C^2 dv); plus, for reference, the recurrence's own count
+    (S k, the rank-one update and S q: 6 dk dv per token and head)."""
+    C = DN_CHUNK
+    chunks = -(-T // C)
+    per = 6 * C * C * dk + 4 * C * C * dv + 6 * C * dk * dv
+    return {"chunked": chunks * H * per, "recurrence": 6 * T * H * dk * dv}
 
 
 def run_deltanet(args, w, K, rank, world, local_rank):
@@ -1046,16 +1069,14 @@ def run_deltanet(args, w, K, rank, world, local_rank):
     ms_full = measure(full, max(1, min(steps, 20)))
     if tg.tg_get_device_status(raise_on_error=False) != 0:
         raise RuntimeError("device status set during the delta rule")
-    props = torch.cuda.get_device_properties(dev)
-    sm_max = clocks.get("sm_max_mhz") or 2032.0
-    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    peaks, peak_src = load_peaks()
     fl = deltanet_flops(M, H, dk, dv)
-    ach = fl / ms_kept / 1e9
+    ach = fl["chunked"] / ms_kept / 1e9
     line = {
         "metric": "Gated-DeltaNet layer over the kept tokens: prompt tokens/s",
         "value": N / (ms_kept * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
         "warmup": warmup, "ms_per_step": ms_kept, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "mode": "deltanet",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "mode": "deltanet",
         "config": {"workload": f"gated delta rule, {H} heads of dk = dv = {dk}, over the kept "
                                f"tokens of {w.name}", "N": N, "K": K, "M": M, "heads": H,
                    "dk": dk, "dv": dv, "inputs": "q, k, v bf16; alpha, beta fp32",
@@ -1063,10 +1084,14 @@ def run_deltanet(args, w, K, rank, world, local_rank):
                    "launch": "direct C-ABI call (chunk preparation + state scan)"},
         "full": {"ms": ms_full, "tokens_per_s": N / (ms_full * 1e-3), "T": N},
         "speedup": ms_full / ms_kept,
-        "roofline": {"kernel": "gated_delta_rule (both kernels)", "bound": "alu",
-                     "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                     "traffic": None, "algorithmic": fl,
-                     "peak_source": "derived: SMs x 128 FP32 lanes x 2 flops x max SM clock"},
+        "roofline": {"kernel": "gated_delta_rule (both kernels)", "bound": "tensor",
+                     "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ach / peaks["bf16_tflops"],
+                     "traffic": ncu_traffic(w.name, "gated_delta_rule"),
+                     "algorithmic": fl["chunked"], "recurrence_flops": fl["recurrence"],
+                     "peak_source": f"{peak_src} (bf16 burst)",
+                     "note": "the state scan is sequential over chunks, one CTA per head: "
+                             f"{H} of the SMs"},
         "gpu_launches": 2 * steps,
         "clocks": clocks,
     }

@@ -97,3 +97,12 @@ def test_backward_work_counts_and_traffic_table():
         fresh = trf["source_sha"] == bench.source_hash(bench.KERNEL_SOURCES[kern])
         assert got == (trf["bytes_per_launch"] if fresh else None)
     assert bench.ncu_traffic(w.name, "no_such_kernel") is None
+
+
+def test_default_workload_traffic_is_current():
+    """The bench's default workload has a DRAM-traffic entry for every kernel
+    of the step, captured from the kernels' current sources (a kernel changed
+    since its capture reports null traffic and fails here until re-captured)."""
+    import bench
+    for kern in bench.KERNELS:
+        assert bench.ncu_traffic(bench.DEFAULT_WORKLOAD, kern) is not None, kern
