@@ -380,6 +380,9 @@ constexpr uint32_t kStageBytes = 10 * kBox;  // 80 KB
 
 struct ScanSmem {
   ScanStage st[2];
+  uint8_t sb[kTile128];    // S as bf16 [128 rows r][128 k], K-major, 128-byte swizzle: A of S W-^T, S Qg^T
+  uint8_t ub[kHalf128];    // U^T as bf16 [128 rows r][64 tokens], same: A of U^T K', U^T P^T
+  uint8_t ost[2 * kBox];   // O of one chunk, [64 tokens][128 dv] as two 64-column boxes, for the TMA store
   uint64_t op_full[2], op_empty[2];
   uint64_t s_ready, u_full, u_ready, s_full, o_full[2], o_free[2];
   uint64_t drain;
@@ -387,10 +390,28 @@ struct ScanSmem {
   int abort;
 };
 
-// TMEM columns: D_S (the fp32 state) [0, 128), S as bf16 [128, 192), D_U
-// [192, 256) with U as bf16 written back over its first 32 columns, D_O
-// double-buffered at [256, 320) and [320, 384).
-constexpr uint32_t kColS = 0, kColSb = 128, kColU = 192, kColO = 256;
+// TMEM columns: D_U [0, 64), D_S' = U^T K' of the chunk [64, 192), D_O
+// double-buffered at [192, 256) and [256, 320).
+constexpr uint32_t kColU = 0, kColSp = 64, kColO = 192;
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the stores committed so far have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... and are complete in global memory
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     dn_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_v,
@@ -398,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_qg,
                       const __grid_constant__ CUtensorMap tm_kp,
                       const __grid_constant__ CUtensorMap tm_t,
-                      const __grid_constant__ CUtensorMap tm_p, int T_len, int H, int n_ch,
+                      const __grid_constant__ CUtensorMap tm_p,
+                      const __grid_constant__ CUtensorMap tm_o, int T_len, int H, int n_ch,
                       const float* __restrict__ gc, const float* __restrict__ S0,
-                      __nv_bfloat16* __restrict__ o, float* __restrict__ S_out,
-                      uint32_t* status) {
+                      float* __restrict__ S_out, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   ScanSmem& S = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -430,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_kp);
     tma_prefetch_desc(&tm_t);
     tma_prefetch_desc(&tm_p);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.tmem_base), 512);
@@ -472,8 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------- MMA
+      // Every operand in shared memory.  Per chunk, in issue order:
+      //   U^T = V^T T^T ; [S ready] U^T += S W-^T ; O^T = S Qg^T ;
+      //   [U ready] S' = U^T K' ; O^T += U^T P^T
+      // so O^T = S Qg^T runs while the row threads round U, and U^T P^T and
+      // the next chunk's V^T T^T while they update S.
       constexpr uint32_t idesc_ut = idesc_bf16_f32(128, 64, 1, 0);   // V^T T^T
-      constexpr uint32_t idesc_sk = idesc_bf16_f32(128, 64, 0, 0);   // S (W-)^T, S Qg^T, U^T P^T
+      constexpr uint32_t idesc_n64 = idesc_bf16_f32(128, 64, 0, 0);  // S W-^T, S Qg^T, U^T P^T
       constexpr uint32_t idesc_up = idesc_bf16_f32(128, 128, 0, 1);  // U^T K'
       const uint64_t vd0 = smem_desc_sw128(smem_u32(S.st[0].v), kBox, 1024);
       const uint64_t wd0 = smem_desc_sw128(smem_u32(S.st[0].wn), 16, 1024);
@@ -481,45 +508,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kd0 = smem_desc_sw128(smem_u32(S.st[0].kp), kBox, 1024);
       const uint64_t td0 = smem_desc_sw128(smem_u32(S.st[0].t), 16, 1024);
       const uint64_t pd0 = smem_desc_sw128(smem_u32(S.st[0].p), 16, 1024);
-      const uint32_t d_u = tmem + kColU, d_s = tmem + kColS, a_s = tmem + kColSb;
+      const uint64_t sd = smem_desc_sw128(smem_u32(S.sb), 16, 1024);
+      const uint64_t ud = smem_desc_sw128(smem_u32(S.ub), 16, 1024);
+      const uint32_t d_u = tmem + kColU, d_s = tmem + kColSp;
       bool ok = true;
       for (int c = 0; ok && c < n_ch; ++c) {
         const int s = c & 1;
         const uint64_t so = static_cast<uint64_t>(s) * (kStageBytes >> 4);
         if (!(ok = mbar_wait(smem_u32(&S.op_full[s]), (c >> 1) & 1, abort, status))) break;
         tc_fence_after();
-        // U^T = V^T T^T (independent of S)
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_ss(d_u, vd0 + so + ((kk * 2048) >> 4), td0 + so + ((kk * 32) >> 4), idesc_ut,
                  kk > 0 ? 1u : 0u);
         if (!(ok = mbar_wait(smem_u32(&S.s_ready), c & 1, abort, status))) break;
         tc_fence_after();
-        // U^T += S (W-)^T
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ts(d_u, a_s + kk * 8, wd0 + so + (((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
-                 idesc_sk, 1u);
+          mma_ss(d_u, sd + (((kk >> 2) * kHalf128 + (kk & 3) * 32) >> 4),
+                 wd0 + so + (((kk >> 2) * kBox + (kk & 3) * 32) >> 4), idesc_n64, 1u);
         mma_commit(smem_u32(&S.u_full));
-        // O^T = S Qg^T into D_O[s], once the chunk two back has been read out
         if (!(ok = mbar_wait(smem_u32(&S.o_free[s]), ((c >> 1) & 1) ^ 1, abort, status))) break;
         tc_fence_after();
         const uint32_t d_o = tmem + kColO + s * 64;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ts(d_o, a_s + kk * 8, qd0 + so + (((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
-                 idesc_sk, kk > 0 ? 1u : 0u);
+          mma_ss(d_o, sd + (((kk >> 2) * kHalf128 + (kk & 3) * 32) >> 4),
+                 qd0 + so + (((kk >> 2) * kBox + (kk & 3) * 32) >> 4), idesc_n64,
+                 kk > 0 ? 1u : 0u);
         if (!(ok = mbar_wait(smem_u32(&S.u_ready), c & 1, abort, status))) break;
         tc_fence_after();
-        // S += U^T K'  (D_S already holds g_C S)
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_ts(d_s, d_u + kk * 8, kd0 + so + ((kk * 2048) >> 4), idesc_up, 1u);
+          mma_ss(d_s, ud + ((kk * 32) >> 4), kd0 + so + ((kk * 2048) >> 4), idesc_up,
+                 kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&S.s_full));
-        // O^T += U^T P^T
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_ts(d_o, d_u + kk * 8, pd0 + so + ((kk * 32) >> 4), idesc_sk, 1u);
+          mma_ss(d_o, ud + ((kk * 32) >> 4), pd0 + so + ((kk * 32) >> 4), idesc_n64, 1u);
         mma_commit(smem_u32(&S.o_full[s]));
         mma_commit(smem_u32(&S.op_empty[s]));
       }
@@ -528,121 +554,121 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------- row threads
-    const int r = threadIdx.x - 128;  // row of S (dv index) = TMEM lane
+    // Thread r owns row r of the state (the dv index, and TMEM lane r) in
+    // fp32 registers for the whole walk.
+    const int r = threadIdx.x - 128;
     const uint32_t lb = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    // 64 state columns (two 32-column pieces) -> D_S = f S there, and their
-    // bf16 pairs into 32 columns of the copy
-    auto put_half = [&](int hf, const uint32_t (&a)[32], const uint32_t (&b)[32], float f) {
-      uint32_t w[32];
+    float sv[kD];
+    if (S0 != nullptr) {
+      const float4* src = reinterpret_cast<const float4*>(S0 + (static_cast<int64_t>(h) * kD + r) * kD);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(a[e]) * f);
-      tmem_st32(tmem + lb + kColS + 64 * hf, w);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(b[e]) * f);
-      tmem_st32(tmem + lb + kColS + 64 * hf + 32, w);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        w[m] = pack_bf16x2(__uint_as_float(a[2 * m]), __uint_as_float(a[2 * m + 1]));
-        w[16 + m] = pack_bf16x2(__uint_as_float(b[2 * m]), __uint_as_float(b[2 * m + 1]));
+      for (int e = 0; e < kD / 4; ++e) {
+        const float4 a = src[e];
+        sv[4 * e] = a.x;
+        sv[4 * e + 1] = a.y;
+        sv[4 * e + 2] = a.z;
+        sv[4 * e + 3] = a.w;
       }
-      tmem_st32(tmem + lb + kColSb + 32 * hf, w);
-    };
-    auto state_ready = [&]() {
-      tmem_st_wait();
-      tc_fence_before();
+    } else {
+#pragma unroll
+      for (int e = 0; e < kD; ++e) sv[e] = 0.f;
+    }
+    // S as bf16 into the swizzled A tile (row r), then hand it over
+    auto put_state = [&]() {
+#pragma unroll
+      for (int c8 = 0; c8 < kD / 8; ++c8) {
+        const uint4 w = make_uint4(pack_bf16x2(sv[8 * c8], sv[8 * c8 + 1]),
+                                   pack_bf16x2(sv[8 * c8 + 2], sv[8 * c8 + 3]),
+                                   pack_bf16x2(sv[8 * c8 + 4], sv[8 * c8 + 5]),
+                                   pack_bf16x2(sv[8 * c8 + 6], sv[8 * c8 + 7]));
+        *reinterpret_cast<uint4*>(S.sb + sw128_offset(r, 8 * c8, kHalf128)) = w;
+      }
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.s_ready));
     };
-    // O^T of chunk cc (lane r: column r of every token of the chunk)
-    auto read_out = [&](int cc) -> bool {
+    // O^T of chunk cc from TMEM (lane r: dv column r of each token) through
+    // shared memory to global memory with one TMA store per 64 columns.  All
+    // four row warps reach both named barriers whatever happened before (a
+    // wait that gave up only skips the work), so none can be left waiting.
+    auto read_out = [&](int cc, bool& ok) {
       const int b = cc & 1;
-      if (!warp_wait(smem_u32(&S.o_full[b]), (cc >> 1) & 1, abort, status)) return false;
-      tc_fence_after();
-      uint32_t u[2][32];
-      tmem_ld32(tmem + lb + kColO + 64 * b, u[0]);
-      tmem_ld32(tmem + lb + kColO + 64 * b + 32, u[1]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.o_free[b]));
-      const int n = min(kC, T_len - cc * kC);
-      __nv_bfloat16* dst = o + (static_cast<int64_t>(cc) * kC * H + h) * kD + r;
+      if (r == 0) bulk_wait_read_all();  // the previous chunk's store has read the staging tile
+      row_sync();
+      if (ok) ok = warp_wait(smem_u32(&S.o_full[b]), (cc >> 1) & 1, abort, status);
+      if (ok) {
+        tc_fence_after();
+        uint32_t u[2][32];
+        tmem_ld32(tmem + lb + kColO + 64 * b, u[0]);
+        tmem_ld32(tmem + lb + kColO + 64 * b + 32, u[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.o_free[b]));
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(S.ost + (r >> 6) * kBox) + (r & 63);
 #pragma unroll
-      for (int i = 0; i < kC; ++i)
-        if (i < n)
-          dst[static_cast<int64_t>(i) * H * kD] = __float2bfloat16_rn(__uint_as_float(u[i >> 5][i & 31]));
-      return true;
-    };
-    {
-      // the initial state: D_S = g_C(0) S0, and S0 as bf16
-      const float g0 = gc[h];
-      const float* src = S0 != nullptr ? S0 + (static_cast<int64_t>(h) * kD + r) * kD : nullptr;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t a[32], b[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          a[e] = src ? __float_as_uint(src[64 * hf + e]) : 0u;
-          b[e] = src ? __float_as_uint(src[64 * hf + 32 + e]) : 0u;
-        }
-        put_half(hf, a, b, g0);
+        for (int i = 0; i < kC; ++i)
+          dst[i * 64] = __float2bfloat16_rn(__uint_as_float(u[i >> 5][i & 31]));
+        fence_proxy_async_smem();
       }
-      state_ready();
-    }
+      row_sync();
+      if (r == 0 && *abort == 0) {
+        tma_store_2d(&tm_o, smem_u32(S.ost), h * kD, cc * kC);
+        tma_store_2d(&tm_o, smem_u32(S.ost) + kBox, h * kD + 64, cc * kC);
+        bulk_commit();
+      }
+    };
+    put_state();
     bool ok = true;
-    for (int c = 0; ok && c < n_ch; ++c) {
-      const float g_next = c + 1 < n_ch ? gc[static_cast<int64_t>(c + 1) * H + h] : 1.f;
-      // U = D_U as bf16, written back over the first 32 columns of D_U
-      if (!(ok = warp_wait(smem_u32(&S.u_full), c & 1, abort, status))) break;
-      tc_fence_after();
-      {
-        uint32_t u[2][32], pk[32];
+    for (int c = 0; c < n_ch; ++c) {
+      const float g_c = gc[static_cast<int64_t>(c) * H + h];
+      // U^T row r as bf16 into its A tile
+      if (ok) ok = warp_wait(smem_u32(&S.u_full), c & 1, abort, status);
+      if (ok) {
+        tc_fence_after();
+        uint32_t u[2][32];
         tmem_ld32(tmem + lb + kColU, u[0]);
         tmem_ld32(tmem + lb + kColU + 32, u[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          pk[m] = pack_bf16x2(__uint_as_float(u[0][2 * m]), __uint_as_float(u[0][2 * m + 1]));
-          pk[16 + m] = pack_bf16x2(__uint_as_float(u[1][2 * m]), __uint_as_float(u[1][2 * m + 1]));
+        for (int c8 = 0; c8 < kC / 8; ++c8) {
+          const uint32_t* x = &u[c8 >> 2][(c8 & 3) * 8];
+          const uint4 w = make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                     pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                     pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                     pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+          *reinterpret_cast<uint4*>(S.ub + sw128_offset(r, 8 * c8, kHalf128)) = w;
         }
-        tmem_st32(tmem + lb + kColU, pk);
-        tmem_st_wait();
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.u_ready));
       }
-      // the previous chunk's output, while this chunk's update runs
-      if (c > 0 && !(ok = read_out(c - 1))) break;
-      // the state after this chunk: its bf16 copy, and g_C S for the next
-      if (!(ok = warp_wait(smem_u32(&S.s_full), c & 1, abort, status))) break;
-      tc_fence_after();
-      if (c + 1 < n_ch) {
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t a[32], b[32];
-          tmem_ld32(tmem + lb + kColS + 64 * hf, a);
-          tmem_ld32(tmem + lb + kColS + 64 * hf + 32, b);
-          tmem_ld_wait();
-          put_half(hf, a, b, g_next);
-        }
-        state_ready();
-      }
-    }
-    if (ok && n_ch > 0) ok = read_out(n_ch - 1);
-    if (ok && S_out != nullptr) {
-      // the final state (the last update left it unscaled in D_S)
-      float* dst = S_out + (static_cast<int64_t>(h) * kD + r) * kD;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lb + kColS + 32 * q, a);
-        tmem_ld_wait();
+      // S <- g_C S + U^T K'
+      if (ok) ok = warp_wait(smem_u32(&S.s_full), c & 1, abort, status);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + 32 * q + e) =
-              make_float4(__uint_as_float(a[e]), __uint_as_float(a[e + 1]),
-                          __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+        for (int q = 0; q < 4; ++q) {
+          uint32_t d[32];
+          tmem_ld32(tmem + lb + kColSp + 32 * q, d);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            sv[32 * q + e] = fmaf(g_c, sv[32 * q + e], __uint_as_float(d[e]));
+        }
+        tc_fence_before();
+        if (c + 1 < n_ch) put_state();
       }
+      // this chunk's output, while the next chunk's products run
+      read_out(c, ok);
+    }
+    if (r == 0) bulk_wait_all();
+    if (ok && S_out != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(S_out + (static_cast<int64_t>(h) * kD + r) * kD);
+#pragma unroll
+      for (int e = 0; e < kD / 4; ++e)
+        dst[e] = make_float4(sv[4 * e], sv[4 * e + 1], sv[4 * e + 2], sv[4 * e + 3]);
     }
   }
   tc_fence_before();
@@ -670,10 +696,12 @@ cudaError_t launch_deltanet_tc(const void* q, const void* k, const void* v, cons
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const uint64_t cols = static_cast<uint64_t>(H) * kD, rows = static_cast<uint64_t>(T_len);
-  CUtensorMap tm_q, tm_k, tm_v, tm_wn, tm_qg, tm_kp, tm_t, tm_p;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_wn, tm_qg, tm_kp, tm_t, tm_p;
   bool good = make_tmap_2d(&tm_q, q, bf, 2, cols, rows, cols * 2, 64, 2 * kC, sw) &&
               make_tmap_2d(&tm_k, k, bf, 2, cols, rows, cols * 2, 64, 2 * kC, sw) &&
-              make_tmap_2d(&tm_v, v, bf, 2, cols, rows, cols * 2, 64, kC, sw);
+              make_tmap_2d(&tm_v, v, bf, 2, cols, rows, cols * 2, 64, kC, sw) &&
+              make_tmap_2d(&tm_o, o, bf, 2, cols, rows, cols * 2, 64, kC,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
   const uint64_t rr = static_cast<uint64_t>(recs) * kC;
   good = good && make_tmap_2d(&tm_wn, rec.wn, bf, 2, kD, rr, kD * 2, 64, kC, sw) &&
          make_tmap_2d(&tm_qg, rec.qg, bf, 2, kD, rr, kD * 2, 64, kC, sw) &&
@@ -682,6 +710,7 @@ cudaError_t launch_deltanet_tc(const void* q, const void* k, const void* v, cons
          make_tmap_2d(&tm_p, rec.p, bf, 2, kC, rr, kC * 2, 64, kC, sw);
   if (!good) return cudaErrorInvalidValue;
   const size_t s1 = sizeof(PrepSmem) + 1024, s2 = sizeof(ScanSmem) + 1024;
+  static_assert(sizeof(ScanSmem) + 1024 <= 232448, "scan shared memory over the 227 KB limit");
   cudaError_t err =
       cudaFuncSetAttribute(dn_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (err != cudaSuccess) return err;
@@ -694,9 +723,8 @@ cudaError_t launch_deltanet_tc(const void* q, const void* k, const void* v, cons
                    alpha, beta, static_cast<int>(T_len), H, n_ch, rec, st);
   if (err != cudaSuccess) return err;
   err = launch_pdl(dn_scan_tc_kernel, dim3(H), dim3(kThreads), s2, stream, 1u, tm_v, tm_wn, tm_qg,
-                   tm_kp, tm_t, tm_p, static_cast<int>(T_len), H, n_ch,
-                   static_cast<const float*>(rec.gc), S0, static_cast<__nv_bfloat16*>(o), S_out,
-                   st);
+                   tm_kp, tm_t, tm_p, tm_o, static_cast<int>(T_len), H, n_ch,
+                   static_cast<const float*>(rec.gc), S0, S_out, st);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
