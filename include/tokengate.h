@@ -108,12 +108,12 @@ tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d,
 /*
  * Bytes of the select workspace (device memory the caller owns, 256-byte
  * aligned, used by tg_select_topk and optionally filled by tg_gate_score):
- * 40 KiB for any N.  It must be zeroed once before its first use
+ * 104 KiB for any N.  It must be zeroed once before its first use
  * (cudaMemset); every tg_select_topk that returns TG_OK and whose kernel
  * finishes without a device error leaves it ready for the next call: its
  * histograms (including one a tg_gate_score put there), header and barrier
- * counter are back at zero (per-CTA counts and a barrier generation word
- * carry over and need no reset), so it can be reused call after call on
+ * counter are back at zero (per-CTA counts, a barrier generation word and
+ * the candidate keys of long spans carry over and need no reset), so it can be reused call after call on
  * one stream.  A tg_gate_score that filled it must be followed by a
  * tg_select_topk on the same workspace before the next tg_gate_score.
  * After TG_ERR_TIMEOUT, zero it again.  Calls that share a workspace must
@@ -159,7 +159,7 @@ tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin,
  * does).  The pages have no counterpart: this is a deployment variant of the
  * select above, with the same arguments (minus the workspace), the same
  * result and the same limits.  It allocates nothing: its scratch is a
- * 40 KiB array compiled into the library, which every GPU that loads the
+ * 104 KiB array compiled into the library, which every GPU that loads the
  * library holds until the process exits.  A call whose scratch would not fit
  * in the array returns TG_ERR_UNSUPPORTED (no N < 2^31 needs more today).
  * The first call on each device looks up that device's array address

@@ -5,7 +5,7 @@
 // with no allocator to draw a buffer from), and on a latency-critical path an
 // allocation is unwelcome anyway: cudaMalloc can synchronise the device and
 // cudaFree does.  This entry point allocates nothing.  Its scratch is the
-// file-scope array below, which every GPU that loads this library holds (40
+// file-scope array below, which every GPU that loads this library holds (104
 // KiB) until the process exits.
 //
 // The array is per device.  Its device address is looked up once per device,
@@ -15,8 +15,8 @@
 // passed to a kernel: the looked-up address is what the kernels get.
 //
 // Every call shares the one array and finds it as the last call left it: each
-// call clears it (cudaMemsetAsync on the caller's stream) before the select
-// kernel runs, so a call that an error interrupted does not poison the next
+// call clears the part that must start at zero (cudaMemsetAsync on the
+// caller's stream) before the select kernel runs, so a call that an error interrupted does not poison the next
 // one.  Calls that overlap on the GPU (on different streams, or concurrent
 // host threads with one device) race on the array and must not be made.
 #include <cuda_runtime.h>
@@ -29,7 +29,7 @@
 namespace tg {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = kSelectWorkspaceBytes;  // 40 KiB
+constexpr size_t kNoAllocScratchBytes = kSelectWorkspaceBytes;  // 104 KiB
 static_assert(sizeof(SelectWorkspace) <= kNoAllocScratchBytes, "scratch holds a select workspace");
 
 // The scratch of tg_select_topk_noalloc (one copy per device).
@@ -86,7 +86,7 @@ extern "C" tg_status tg_select_topk_noalloc(const float* scores, int64_t N, int6
   if (e != cudaSuccess)
     return tg::fail(TG_ERR_CUDA, "select noalloc: scratch address: %s", cudaGetErrorString(e));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(ws, 0, tg::kNoAllocScratchBytes, st);
+  e = cudaMemsetAsync(ws, 0, tg::kSelectZeroedBytes, st);  // the candidate area needs no clearing
   if (e == cudaSuccess)
     e = tg::launch_select(scores, N, doc_begin, doc_end, K, kept_idx,
                           static_cast<tg::SelectWorkspace*>(ws), st);

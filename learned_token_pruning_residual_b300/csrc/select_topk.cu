@@ -65,10 +65,14 @@ struct SelShared {
   uint32_t hist[2048];
   uint32_t warp_a[kWarps];
   uint32_t warp_b[kWarps];
+  uint32_t seg_n[kSelectMaxCtas];    // candidates of each CTA
+  uint32_t seg_off[kSelectMaxCtas];  // their offsets in the gathered list
   uint32_t found_prefix, found_krem;
   uint32_t gt_base, eq_base;
+  uint32_t cand_n, cand_total;
   int nan_seen;
   int abort;
+  int overflow;
 };
 
 // Inclusive sum over the block of one value per thread; returns this
@@ -137,6 +141,7 @@ __device__ __forceinline__ bool grid_barrier(SelectWorkspace* ws, uint32_t nctas
 // Finds, in the merged histogram h of `bins` bins, the bin where the krem-th
 // largest key falls (counting from the top bin down); writes the bin and the
 // rank left inside it to S.found_prefix / S.found_krem.
+template <bool GLOBAL = true>
 __device__ __forceinline__ void find_threshold_bin(const uint32_t* h, int bins, uint32_t krem,
                                                    SelShared& S) {
   const int per = bins / kThreads;  // 4 (2048 bins) or 2 (1024 bins)
@@ -144,7 +149,8 @@ __device__ __forceinline__ void find_threshold_bin(const uint32_t* h, int bins, 
   uint32_t c[4] = {0, 0, 0, 0};
   uint32_t sum = 0;
   for (int k = 0; k < per; ++k) {
-    c[k] = __ldcg(h + bins - 1 - (per * threadIdx.x + k));
+    const uint32_t* p = h + bins - 1 - (per * threadIdx.x + k);
+    c[k] = GLOBAL ? __ldcg(p) : *p;
     sum += c[k];
   }
   uint32_t total;
@@ -205,10 +211,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   {
     int nan_local = 0;
-    for (int i = tid; i < n; i += kThreads) {
-      const float s = __ldg(src + i);
-      nan_local |= (s != s);
-      if constexpr (CACHED) keys_smem[i] = key_of(s);
+    constexpr int kLoadBatch = 16;  // loads in flight per thread before their stores
+    for (int i0 = tid; i0 < n; i0 += kLoadBatch * kThreads) {
+      float v[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int i = i0 + u * kThreads;
+        v[u] = i < n ? __ldg(src + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int i = i0 + u * kThreads;
+        nan_local |= (v[u] != v[u]);
+        if constexpr (CACHED) {
+          if (i < n) keys_smem[i] = key_of(v[u]);
+        }
+      }
     }
     if (__any_sync(0xffffffffu, nan_local) && lane == 0) S.nan_seen = 1;
   }
@@ -217,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint32_t T = 0, k_eq = 0;
   bool ok = true;
+  bool fast = false;  // the candidate path found T and this CTA's offsets
   const bool trivial = K == 0 || K == D;
   if (K == 0) {
     T = 0xFFFFFFFFu;  // nothing is above, and no tie is taken
@@ -226,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---- three radix passes: 11, 11, 10 bits
     uint32_t prefix = 0, krem = static_cast<uint32_t>(K);
-#pragma unroll 1
-    for (int pass = 0; pass < 3 && ok; ++pass) {
+    int pass = 0;
+    auto global_pass = [&]() {
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const int bins = pass == 2 ? 1024 : 2048;
       const int pshift = shift + (pass == 2 ? 10 : 11);  // bits above the digit
@@ -246,12 +265,126 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c) atomicAdd(gh + i, c);
         }
         ok = grid_barrier(ws, G, status, S);
-        if (!ok) break;
+        if (!ok) return;
       }
       find_threshold_bin(gh, bins, krem, S);
       prefix = (prefix << (pass == 2 ? 10 : 11)) | S.found_prefix;
       krem = S.found_krem;
+    };
+    global_pass();
+    pass = 1;
+    if constexpr (CACHED) {
+      // ---- candidates: the keys whose first digit is the threshold bin.
+      // Each CTA appends its own to its segment of the workspace and counts
+      // the keys above the bin; after one barrier every CTA gathers all
+      // candidates and finishes the select on them alone: the last two
+      // passes, and the (> T, == T) counts of the lower-ranked CTAs.
+      if (ok) {
+        const uint32_t capc = static_cast<uint32_t>(kSelectCandCap) / G;
+        uint32_t* seg = ws->cand + static_cast<size_t>(cta) * capc;
+        // per-thread counts of candidates and of keys above the bin (packed
+        // as cand + above << 16; each at most a slice), one block scan, then
+        // each thread writes its candidates at its offset
+        uint32_t packed = 0;
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t top = keys_smem[i] >> 21;
+          packed += (top == prefix ? 1u : 0u) + (top > prefix ? 0x10000u : 0u);
+        }
+        uint32_t tot;
+        const uint32_t incl = block_inclusive_scan(packed, S.warp_a, &tot);
+        uint32_t pos = (incl - packed) & 0xFFFFu;
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t k = keys_smem[i];
+          if ((k >> 21) == prefix) {
+            if (pos < capc) __stcg(seg + pos, k);
+            ++pos;
+          }
+        }
+        if (tid == 0) {
+          __stcg(&ws->cnt[cta][0], tot >> 16);
+          __stcg(&ws->cnt[cta][1], tot & 0xFFFFu);
+        }
+        ok = grid_barrier(ws, G, status, S);
+      }
+      if (ok) {
+        const uint32_t capc = static_cast<uint32_t>(kSelectCandCap) / G;
+        // every CTA's counts; candidate offsets; keys above the bin in the
+        // lower-ranked CTAs
+        const uint32_t cn = tid < static_cast<int>(G) ? __ldcg(&ws->cnt[tid][1]) : 0u;
+        const uint32_t an = tid < cta ? __ldcg(&ws->cnt[tid][0]) : 0u;
+        if (tid == 0) S.overflow = 0;
+        __syncthreads();
+        if (cn > capc) S.overflow = 1;
+        uint32_t total, an_tot;
+        const uint32_t off = block_inclusive_scan(cn, S.warp_a, &total) - cn;
+        block_inclusive_scan(an, S.warp_b, &an_tot);
+        if (tid < static_cast<int>(G)) {
+          S.seg_n[tid] = cn;
+          S.seg_off[tid] = off;
+        }
+        if (tid == 0) S.cand_total = total;
+        __syncthreads();
+        if (!S.overflow) {
+          uint32_t* cand_smem = keys_smem + ((slice + 3) & ~3);
+          const uint32_t nc = S.cand_total;
+          // gather: warp w copies segments w, w + 16, ...; eight loads in
+          // flight per lane before their stores
+          constexpr int kBatch = 8;
+          for (uint32_t sg = tid >> 5; sg < G; sg += kWarps) {
+            const uint32_t ns = S.seg_n[sg], off = S.seg_off[sg];
+            const uint32_t* src2 = ws->cand + static_cast<size_t>(sg) * capc;
+            for (uint32_t j0 = lane; j0 < ns; j0 += kBatch * 32) {
+              uint32_t v[kBatch];
+#pragma unroll
+              for (int u = 0; u < kBatch; ++u) {
+                const uint32_t j = j0 + u * 32;
+                v[u] = j < ns ? __ldcg(src2 + j) : 0u;
+              }
+#pragma unroll
+              for (int u = 0; u < kBatch; ++u) {
+                const uint32_t j = j0 + u * 32;
+                if (j < ns) cand_smem[off + j] = v[u];
+              }
+            }
+          }
+          __syncthreads();
+          for (; pass < 3; ++pass) {
+            const int shift = pass == 1 ? 10 : 0;
+            const int bins = pass == 2 ? 1024 : 2048;
+            const int pshift = shift + (pass == 2 ? 10 : 11);
+            for (int i = tid; i < bins; i += kThreads) S.hist[i] = 0;
+            __syncthreads();
+            for (uint32_t i = tid; i < nc; i += kThreads) {
+              const uint32_t k = cand_smem[i];
+              if ((k >> pshift) == prefix)
+                atomicAdd(&S.hist[(k >> shift) & static_cast<uint32_t>(bins - 1)], 1u);
+            }
+            __syncthreads();
+            find_threshold_bin<false>(S.hist, bins, krem, S);
+            prefix = (prefix << (pass == 2 ? 10 : 11)) | S.found_prefix;
+            krem = S.found_krem;
+          }
+          // (> T, == T) among the lower-ranked CTAs' candidates, packed as
+          // gt + eq << 16 (each at most kSelectCandCap)
+          const uint32_t T2 = prefix;
+          uint32_t packed = 0;
+          const uint32_t lower = S.seg_off[cta];
+          for (uint32_t i = tid; i < lower; i += kThreads) {
+            const uint32_t k = cand_smem[i];
+            packed += (k > T2 ? 1u : 0u) + (k == T2 ? 0x10000u : 0u);
+          }
+          uint32_t packed_tot;
+          block_inclusive_scan(packed, S.warp_a, &packed_tot);
+          if (tid == 0) {
+            S.gt_base = an_tot + (packed_tot & 0xFFFFu);
+            S.eq_base = packed_tot >> 16;
+          }
+          __syncthreads();
+          fast = true;
+        }
+      }
     }
+    for (; ok && pass < 3; ++pass) global_pass();
     T = prefix;
     k_eq = krem;
   }
@@ -272,9 +405,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         eq += k == T;
       }
     }
-    uint32_t gt_tot, eq_tot;
-    const uint32_t gt_incl = block_inclusive_scan(gt, S.warp_a, &gt_tot);
-    const uint32_t eq_incl = block_inclusive_scan(eq, S.warp_b, &eq_tot);
+    uint32_t gt_tot, eq_tot, gt_incl, eq_incl;
+    if constexpr (CACHED) {
+      // one scan of gt + eq << 16 (each at most a cached slice, <= 24576 keys)
+      uint32_t pk_tot;
+      const uint32_t pk_incl = block_inclusive_scan(gt | (eq << 16), S.warp_a, &pk_tot);
+      gt_tot = pk_tot & 0xFFFFu;
+      eq_tot = pk_tot >> 16;
+      gt_incl = pk_incl & 0xFFFFu;
+      eq_incl = pk_incl >> 16;
+    } else {
+      gt_incl = block_inclusive_scan(gt, S.warp_a, &gt_tot);
+      eq_incl = block_inclusive_scan(eq, S.warp_b, &eq_tot);
+    }
     if (trivial) {
       // K == D: the kept document tokens are the whole span, position = offset
       if (tid == 0) {
@@ -282,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         S.eq_base = static_cast<uint32_t>(lo);
       }
       __syncthreads();
+    } else if (fast) {
+      // S.gt_base / S.eq_base were set from the candidates
     } else {
       if (tid == 0) {
         __stcg(&ws->cnt[cta][0], gt_tot);
@@ -308,22 +453,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       uint32_t gt_before = gt_incl - gt + S.gt_base, eq_before = eq_incl - eq + S.eq_base;
+      bool bad = false;
       for (int i = r0; i < r1; ++i) {
         const uint32_t k = K == D ? 0u : load_key(i);
         const bool is_gt = K != D && k > T;
         const bool is_eq = K == D || k == T;
         const bool keep = is_gt || (is_eq && eq_before < k_eq);
-        if (keep) {
-          const uint32_t pos = gt_before + min(eq_before, k_eq);
-          if (pos < static_cast<uint32_t>(K)) {
-            idx[b + pos] = b + lo + i;
-          } else {
-            atomicOr(status, kStatusBadIndex);  // cannot happen for a consistent threshold
-          }
-        }
+        const uint32_t pos = gt_before + min(eq_before, k_eq);
+        bad |= keep && pos >= static_cast<uint32_t>(K);
+        if (keep && pos < static_cast<uint32_t>(K)) idx[b + pos] = b + lo + i;
         gt_before += is_gt;
         eq_before += is_eq;
       }
+      if (bad) atomicOr(status, kStatusBadIndex);  // cannot happen for a consistent threshold
     }
   }
 
@@ -609,10 +751,10 @@ cudaError_t launch_select(const float* scores, int64_t N, int64_t b, int64_t e, 
   uint32_t* status = device_status_word();
   if (status == nullptr) return cudaErrorInvalidDevice;
   if (slice <= kCacheKeys) {
-    const size_t smem = static_cast<size_t>(slice > 0 ? slice : 1) * 4;
+    const size_t smem = (static_cast<size_t>((slice + 3) & ~3) + kSelectCandCap) * 4;
     cudaError_t err = cudaFuncSetAttribute(select_topk_kernel<true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kCacheKeys * 4);
+                                           (kCacheKeys + kSelectCandCap) * 4);
     if (err != cudaSuccess) return err;
     err = launch_pdl(select_topk_kernel<true>, dim3(G), dim3(kThreads), smem, stream, 1u, scores,
                      (int)N, (int)b, (int)e, (int)K, idx, status, ws, slice);

@@ -2,6 +2,8 @@
 // launchers, tensor-map helpers and error reporting.
 #pragma once
 
+#include <cstddef>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -63,14 +65,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // its first use; every successful select call leaves it zeroed again)
 constexpr int kSelectMaxCtas = 256;
 constexpr uint32_t kSelectHistMagic = 0x74676831u;  // header stamp of a gate-filled histogram
+// Candidate keys (those in the first digit's threshold bin) that the
+// multi-CTA select can keep in the workspace: with them its second and third
+// passes and the per-CTA counts are local, after one grid barrier.
+constexpr int kSelectCandCap = 16384;
 struct SelectWorkspace {
   uint32_t hist[3][2048];           // radix histograms of the select's three passes
   uint32_t gate_hist[2048];         // the first pass, counted by the gate epilogue
-  uint32_t cnt[kSelectMaxCtas][2];  // per-CTA (> T, == T) counts for the ordered compaction
+  uint32_t cnt[kSelectMaxCtas][2];  // per-CTA counts exchanged between the CTAs
   uint32_t hdr[4];                  // {magic, N, doc_begin, doc_end} when the gate filled gate_hist
   uint32_t bar_count, bar_gen;      // grid barrier: arrivals, generation
+  uint32_t cand[kSelectCandCap];    // candidate keys, per-CTA segments; written before read
 };
-constexpr size_t kSelectWorkspaceBytes = 40960;
+// Everything before `cand` must start at zero; `cand` needs no clearing.
+constexpr size_t kSelectZeroedBytes = offsetof(SelectWorkspace, cand);
+constexpr size_t kSelectWorkspaceBytes = 40960 + 4 * static_cast<size_t>(kSelectCandCap);
+static_assert(kSelectZeroedBytes <= 40960, "select workspace: zeroed part");
 static_assert(sizeof(SelectWorkspace) <= kSelectWorkspaceBytes, "select workspace");
 // Spans up to this many keys take the single-CTA select (all keys cached in
 // shared memory, no grid barrier); longer spans the multi-CTA one, whose
