@@ -275,8 +275,8 @@ __device__ __forceinline__ void softmax_epilogue(AttnSmem& S, const AttnArgs& ar
 template <bool BIAS, int NH>
 __device__ __forceinline__ void mma_loop(AttnSmem& S, const AttnArgs& args, uint32_t tmem,
                                          int nloc, const uint64_t (&qd)[2][kDH / 16],
-                                         const uint64_t (&kd0)[2], const uint64_t (&qxd)[2],
-                                         const uint64_t (&kxd)[2], const uint64_t (&vd0)[2],
+                                         uint64_t kd0, const uint64_t (&qxd)[2], uint64_t kxd0,
+                                         uint64_t vd0,
                                          volatile int* abort) {
   constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);  // Q K^T, both K-major
   constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // P V, V MN-major
@@ -304,7 +304,7 @@ __device__ __forceinline__ void mma_loop(AttnSmem& S, const AttnArgs& args, uint
         tc_fence_after();
         const uint32_t o_tmem = tmem + 256 + t * 128;
         const uint32_t p_tmem = tmem + t * 128;
-        const uint64_t vd = vd0[sp];
+        const uint64_t vd = vd0 + static_cast<uint64_t>(sp) * (kTileBytes >> 4);
         mma_ts(o_tmem, p_tmem, vd, idesc_o, ip > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kBK / 16; ++kk)
@@ -313,14 +313,14 @@ __device__ __forceinline__ void mma_loop(AttnSmem& S, const AttnArgs& args, uint
         if (t == NH - 1) mma_commit(smem_u32(&S.v_empty[sp]));
       }
       if (i < nloc) {
-        const uint64_t kd = kd0[s];
+        const uint64_t kd = kd0 + static_cast<uint64_t>(s) * (kTileBytes >> 4);
         const uint32_t s_tmem = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kDH / 16; ++kk)
           mma_ss(s_tmem, qd[t][kk],
                  kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
                  kk > 0 ? 1u : 0u);
-        if (BIAS) mma_ss(s_tmem, qxd[t], kxd[s], idesc_s, 1u);
+        if (BIAS) mma_ss(s_tmem, qxd[t], kxd0 + static_cast<uint64_t>(s) * (kXBytes >> 4), idesc_s, 1u);
         mma_commit(smem_u32(&S.s_full[t]));
       }
     }
@@ -474,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kDH / 16; ++kk)
             qd[t][kk] = smem_desc_sw128(smem_u32(S.q[t]) + (kk >> 2) * kHalfBytes + (kk & 3) * 32,
                                         16, 1024);
-        const uint64_t kd0[2] = {smem_desc_sw128(smem_u32(S.k[0]), 16, 1024),
-                                 smem_desc_sw128(smem_u32(S.k[1]), 16, 1024)};
+        // stage 1 of each ring is a constant added to the start-address
+        // field (address >> 4; the sum stays below 256 KB, so it never
+        // carries): no runtime-indexed arrays, which would live in local memory
+        const uint64_t kd0 = smem_desc_sw128(smem_u32(S.k[0]), 16, 1024);
         const uint64_t qxd[2] = {smem_desc_noswizzle(smem_u32(S.qx[0]), kXLbo, kXSbo),
                                  smem_desc_noswizzle(smem_u32(S.qx[1]), kXLbo, kXSbo)};
-        const uint64_t kxd[2] = {smem_desc_noswizzle(smem_u32(S.kx[0]), kXLbo, kXSbo),
-                                 smem_desc_noswizzle(smem_u32(S.kx[1]), kXLbo, kXSbo)};
-        const uint64_t vd0[2] = {smem_desc_sw128(smem_u32(S.v[0]), kHalfBytes, 1024),
-                                 smem_desc_sw128(smem_u32(S.v[1]), kHalfBytes, 1024)};
+        const uint64_t kxd = smem_desc_noswizzle(smem_u32(S.kx[0]), kXLbo, kXSbo);
+        const uint64_t vd0 = smem_desc_sw128(smem_u32(S.v[0]), kHalfBytes, 1024);
         if (nh == 2) {
           mma_loop<BIAS, 2>(S, args, tmem, nloc, qd, kd0, qxd, kxd, vd0, abort);
         } else {
