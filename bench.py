@@ -56,35 +56,35 @@ KERNEL_SOURCES = {"gate_score": ("gemm_tc.cu",), "select_topk": ("select_topk.cu
 # hex) of the kernel's source at capture time; a stale hash reports null.
 NCU_TRAFFIC: dict[str, dict] = {
     # Qwen3-1.7B shapes, N = 16384, 10% of the document kept (M = 1868)
-    "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68191232 + 3328,
+    "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68190720 + 17920,
                                           "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 103424,
-                                           "source_sha": "eff82ff787cf8a1d"},
+    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 104192,
+                                           "source_sha": "c3208e678d219762"},
     "qwen3_1p7b_n16k_keep10/gather_rows": {"bytes_per_launch": 7729152,
                                            "source_sha": "27ffa82b44661223"},
-    "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24454656,
+    "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24450304,
                                         "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15368704,
-                                            "source_sha": "6290768b50105383"},
+    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15369984,
+                                            "source_sha": "8bc1c092efcd9386"},
     # N = 131072, 6.25% of the document kept (M = 8432)
-    "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537969664 + 328960,
+    "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537975808 + 367616,
                                              "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n128k_keep6p25/select_topk": {"bytes_per_launch": 576512,
-                                              "source_sha": "eff82ff787cf8a1d"},
-    "qwen3_1p7b_n128k_keep6p25/gather_rows": {"bytes_per_launch": 35033344 + 46848,
+    "qwen3_1p7b_n128k_keep6p25/select_topk": {"bytes_per_launch": 590592,
+                                              "source_sha": "c3208e678d219762"},
+    "qwen3_1p7b_n128k_keep6p25/gather_rows": {"bytes_per_launch": 35035136 + 19968,
                                               "source_sha": "27ffa82b44661223"},
-    "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51425536 + 20341760,
+    "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51419648 + 20432896,
                                            "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69795072 + 3588352,
-                                               "source_sha": "6290768b50105383"},
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69652992 + 3341568,
+                                               "source_sha": "8bc1c092efcd9386"},
     # the backward's bias-gradient kernel at M = 8432
     "qwen3_1p7b_n128k_keep6p25/keybias_bias_grad": {"bytes_per_launch": 137630464 + 3417344,
                                                     "source_sha": "3d91e7a27c9845f8"},
     # the delta rule over the 3507 kept tokens of the 32k prompt (10% budget),
     # both kernels of one call: chunk preparation + state scan
     "qwen3_1p7b_n32k_sweep/gated_delta_rule": {
-        "bytes_per_launch": (29939456 + 6322688) + (72099328 + 3732480),
-        "source_sha": "4c12a2907c700e2b"},
+        "bytes_per_launch": (29793024 + 3418880) + (72087296 + 1477376),
+        "source_sha": "aba62d04c57a9dfb"},
 }
 
 
