@@ -108,6 +108,22 @@ def algorithmic_work(w: TI.Workload, K: int) -> dict:
     }
 
 
+def tensor_peak(peaks: dict, clocks: dict | None) -> tuple[float, str]:
+    """The bf16 denominator for a contraction timed in this run: the burst
+    figure while the SMs held their clock, the sustained one (a seconds-long
+    GEMM loop under the power cap) when the run was power-capped or its
+    median SM clock fell below 97% of the maximum."""
+    capped = False
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        capped = ("sw_power_cap" in (clocks.get("reasons") or [])
+                  or clocks["sm_mhz"] < 0.97 * clocks["sm_max_mhz"])
+    if capped:
+        return peaks["bf16_tflops_sustained"], (
+            f"bf16 sustained: this run was power-capped, median SM clock "
+            f"{clocks['sm_mhz']:.0f} of {clocks['sm_max_mhz']:.0f} MHz")
+    return peaks["bf16_tflops"], "bf16 burst"
+
+
 def load_peaks() -> tuple[dict, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -625,14 +641,15 @@ def run_gpu(args, w, K, rank, world, local_rank):
     dom = max(KERNELS, key=lambda n: kernels[n]["ms"])
     wk = work[dom]
     ms = kernels[dom]["ms"]
+    tpeak, tpeak_kind = tensor_peak(peaks, clocks)
     if wk["bound"] == "tensor":
-        ach, peak, unit = wk["flops"] / ms / 1e9, peaks["bf16_tflops"], "TFLOP/s"
+        ach, peak, unit = wk["flops"] / ms / 1e9, tpeak, "TFLOP/s"
     else:
         ach, peak, unit = wk["bytes"] / ms / 1e6, peaks["hbm_gbs"], "GB/s"
     roofline = {"kernel": dom, "bound": wk["bound"], "achieved": ach, "peak": peak,
                 "unit": unit, "frac": ach / peak, "traffic": ncu_traffic(w.name, dom),
                 "algorithmic": wk["flops"] if wk["bound"] == "tensor" else wk["bytes"],
-                "peak_source": f"{peak_src} ({'bf16 burst' if unit == 'TFLOP/s' else 'HBM copy'})"}
+                "peak_source": f"{peak_src} ({tpeak_kind if unit == 'TFLOP/s' else 'HBM copy'})"}
     pipe_bytes = sum(work[n]["bytes"] for n in PIPELINE)
     pipe_ms = sum(kernels[n]["ms"] for n in PIPELINE)
     pipeline = {"kernels": list(PIPELINE), "bytes": pipe_bytes, "ms": pipe_ms,
@@ -654,7 +671,7 @@ def run_gpu(args, w, K, rank, world, local_rank):
         "roofline": roofline,
         "pipeline": pipeline,
         "attn_tflops": attn["TFLOP/s"],
-        "attn_frac_bf16_peak": attn["TFLOP/s"] / peaks["bf16_tflops"],
+        "attn_frac_bf16_peak": attn["TFLOP/s"] / tpeak,
         "kernels": kernels,
         "instrumented_ms_per_step": float(inst_ms.mean()) if inst_ms is not None else None,
         "e2e": {"value": aggregate_tokens_per_s(w.N, world, e2e_ms), "unit": "tokens/s",
@@ -949,6 +966,7 @@ def run_backward(args, w, K, rank, world, local_rank):
     wk, ms = work["keybias_bias_grad"], kernels["keybias_bias_grad"]["ms"]
     ach = wk["flops"] / ms / 1e9
     traffic = ncu_traffic(w.name, "keybias_bias_grad")
+    tpeak, tpeak_kind = tensor_peak(peaks, clocks)
     line = {
         "metric": "token-gated attention backward to the scorer: prompt tokens/s",
         "value": w.N / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
@@ -959,9 +977,9 @@ def run_backward(args, w, K, rank, world, local_rank):
                    "l2": "flushed between steps (256 MiB write), outside the timed events",
                    "launch": "direct C-ABI calls, an event before and after each"},
         "roofline": {"kernel": "keybias_bias_grad", "bound": "tensor", "achieved": ach,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
-                     "algorithmic": wk["flops"], "peak_source": f"{peak_src} (bf16 burst)"},
+                     "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": ach / tpeak, "traffic": traffic,
+                     "algorithmic": wk["flops"], "peak_source": f"{peak_src} ({tpeak_kind})"},
         "kernels": kernels,
         "gpu_launches": len(calls) * steps,
         "clocks": clocks,
@@ -1070,6 +1088,7 @@ def run_deltanet(args, w, K, rank, world, local_rank):
     if tg.tg_get_device_status(raise_on_error=False) != 0:
         raise RuntimeError("device status set during the delta rule")
     peaks, peak_src = load_peaks()
+    tpeak, tpeak_kind = tensor_peak(peaks, clocks)
     fl = deltanet_flops(M, H, dk, dv)
     ach = fl["chunked"] / ms_kept / 1e9
     line = {
@@ -1085,11 +1104,11 @@ def run_deltanet(args, w, K, rank, world, local_rank):
         "full": {"ms": ms_full, "tokens_per_s": N / (ms_full * 1e-3), "T": N},
         "speedup": ms_full / ms_kept,
         "roofline": {"kernel": "gated_delta_rule (both kernels)", "bound": "tensor",
-                     "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ach / peaks["bf16_tflops"],
+                     "achieved": ach, "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": ach / tpeak,
                      "traffic": ncu_traffic(w.name, "gated_delta_rule"),
                      "algorithmic": fl["chunked"], "recurrence_flops": fl["recurrence"],
-                     "peak_source": f"{peak_src} (bf16 burst)",
+                     "peak_source": f"{peak_src} ({tpeak_kind})",
                      "note": "the state scan is sequential over chunks, one CTA per head: "
                              f"{H} of the SMs"},
         "gpu_launches": 2 * steps,

@@ -106,3 +106,19 @@ def test_default_workload_traffic_is_current():
     import bench
     for kern in bench.KERNELS:
         assert bench.ncu_traffic(bench.DEFAULT_WORKLOAD, kern) is not None, kern
+
+
+def test_tensor_peak_follows_the_clock_record():
+    """A run that held its SM clock is measured against the burst bf16 peak;
+    one that was power-capped (or ran well below the maximum clock) against
+    the sustained one, and the line says which."""
+    import bench
+    peaks = {"bf16_tflops": 1755.4, "bf16_tflops_sustained": 1377.5, "hbm_gbs": 6484.9}
+    assert bench.tensor_peak(peaks, {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0,
+                                     "reasons": []})[0] == 1755.4
+    assert bench.tensor_peak(peaks, None)[0] == 1755.4
+    p, why = bench.tensor_peak(peaks, {"sm_mhz": 1762.0, "sm_max_mhz": 2032.0,
+                                       "reasons": ["sw_power_cap"]})
+    assert p == 1377.5 and "sustained" in why
+    assert bench.tensor_peak(peaks, {"sm_mhz": 1900.0, "sm_max_mhz": 2032.0,
+                                     "reasons": []})[0] == 1377.5
