@@ -64,8 +64,8 @@ NCU_TRAFFIC: dict[str, dict] = {
                                            "source_sha": "27ffa82b44661223"},
     "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24450304,
                                         "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15369984,
-                                            "source_sha": "8bc1c092efcd9386"},
+    "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15368832,
+                                            "source_sha": "bb0705b0fbb4efc2"},
     # N = 131072, 6.25% of the document kept (M = 8432)
     "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537975808 + 367616,
                                              "source_sha": "0f25d4a8caaef008"},
@@ -75,16 +75,16 @@ NCU_TRAFFIC: dict[str, dict] = {
                                               "source_sha": "27ffa82b44661223"},
     "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51419648 + 20432896,
                                            "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69652992 + 3341568,
-                                               "source_sha": "8bc1c092efcd9386"},
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69523840 + 6183936,
+                                               "source_sha": "bb0705b0fbb4efc2"},
     # the backward's bias-gradient kernel at M = 8432
     "qwen3_1p7b_n128k_keep6p25/keybias_bias_grad": {"bytes_per_launch": 137630464 + 3417344,
                                                     "source_sha": "3d91e7a27c9845f8"},
     # the delta rule over the 3507 kept tokens of the 32k prompt (10% budget),
     # both kernels of one call: chunk preparation + state scan
     "qwen3_1p7b_n32k_sweep/gated_delta_rule": {
-        "bytes_per_launch": (29793024 + 3418880) + (72087296 + 1477376),
-        "source_sha": "aba62d04c57a9dfb"},
+        "bytes_per_launch": (29930240 + 3514368) + (72087296 + 1188864),
+        "source_sha": "8d0ec53ce4a61ce6"},
 }
 
 

@@ -394,25 +394,6 @@ struct ScanSmem {
 // double-buffered at [192, 256) and [256, 320).
 constexpr uint32_t kColU = 0, kColSp = 64, kColO = 192;
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
-                                             int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// the stores committed so far have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// ... and are complete in global memory
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     dn_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_wn,

@@ -17,28 +17,34 @@
 // current unit's epilogue.
 //
 // Per CTA (384 threads):
-//   warp 0      TMA: Q of each unit, the K_j ring (2 stages, 128 x 128
-//               bf16, 128-byte swizzle) and the bias inputs ls_j;
-//   warp 3      TMA: the V_j ring (its own thread, so that a V fill, which
-//               waits for the P V two tiles back, never delays a K fill).
-//   warp 1      one thread issues tcgen05.mma:
-//                 S_g = Q K_j^T (+ the bias block) into S[g % 2] (SS form),
-//                 O_A += P_A V_j[0:64), O_B += P_B V_j[64:128) (TS form,
-//                 P read from TMEM).  Q K^T of tile g+1 is issued before
-//                 P V of tile g, so it overlaps the softmax of tile g.
+//   warp 0      TMA: Q of each unit, the K_j ring (3 stages) and V_j ring
+//               (2 stages; 128 x 128 bf16, 128-byte swizzle; V one tile
+//               behind K);
+//   warp 1      one thread issues S_g = Q K_j^T (+ the bias block) into
+//               S[g % 2] (SS form) as soon as K_j is in and the softmax has
+//               loaded S of tile g - 2 (so Q K^T runs up to two tiles ahead
+//               of the softmax);
+//   warp 3      one thread issues O += P_g V_j (TS form, P read from TMEM)
+//               as soon as the softmax has written P_g.
+//               The thread issuing tcgen05.mma waits for the tensor pipe to
+//               take each one, and a barrier wait between two MMAs idles the
+//               pipe for about 100 cycles (B300: the 17 MMAs of a tile take
+//               1090 cycles back to back; one thread with five waits per
+//               tile took 1750-2150).  With Q K^T and P V on two threads,
+//               each thread's waits are covered by the other's MMAs.
 //   warp 2      writes each key tile's bias into one extra K = 16 block of
 //               the Q K^T product (g_h ls_j sqrt(dh) / t as bf16 hi + lo in
 //               two columns; Q holds ones there), so S already carries it.
 //   warps 4-7   softmax A: key columns 0..63 of every tile, one query row
 //   warps 8-11  softmax B: key columns 64..127     per thread.
-// Each half keeps its own running max and sum and its own O accumulator
-// (O_A, O_B), so the two halves never exchange anything per tile; the
-// epilogue merges them once per unit:
-//   o = (O_A 2^(m_A - m) + O_B 2^(m_B - m)) / (l_A 2^(m_A - m) + l_B 2^(m_B - m)).
-// A half's running max is only raised when its max grows by more than 2^8
-// (log2 units); O_A / O_B is then rescaled in TMEM, after the previous
-// tile's P V has completed (pv_done).  TMEM (512 columns): S_0 | S_1 | O_A |
-// O_B; P_A (bf16 pairs) overwrites S columns 0..31, P_B columns 64..95.
+// The two halves of a row share one running max (each tile they swap their
+// 64-column maxima through shared memory) and accumulate into one O; each
+// keeps its own partial row sum, added in the epilogue.  The max is only
+// raised when a row's max grows by more than 2^8 (log2 units); O is then
+// rescaled in TMEM (each half its 64 columns of it) after the previous
+// tile's P V has completed.  TMEM (512 columns): S_0 | S_1 | O | P_0 | P_1;
+// P has buffers of its own, so a Q K^T may overwrite S as soon as the
+// softmax has it in registers, without waiting for the P V that follows.
 #include <algorithm>
 
 #include "tg_device.cuh"
@@ -53,6 +59,17 @@ constexpr int kDH = 128;
 constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = kBK * kDH * 2;   // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
+// The K ring is 3 deep: a K fill waits for the Q K^T of the tile three
+// back, so one fill's TMA latency (1.5-3k cycles with every SM loading) spans
+// two tiles of work.  With 2 stages the fill of K_{g+2} only starts when Q
+// K^T of tile g is done, and that latency set the tile rate.  Q is
+// single-buffered to make room (the next unit's Q loads once the current
+// unit's last Q K^T is done).
+constexpr int kKStages = 3;
+// TMEM columns: S_0 | S_1 (128 fp32 each) | O (128 fp32) | P_0 | P_1 (64
+// columns of bf16 pairs each: half A's 64 keys, then half B's)
+constexpr uint32_t kOCol = 256;
+constexpr uint32_t kPCol = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -71,6 +88,7 @@ struct Attn1hArgs {
   float scale2;      // t / sqrt(dh) * log2(e), > 0
   float bias_scale;  // sqrt(dh) / t: the bias in units of the q.k product
   const float* gain;
+  const float* logsig;  // per kept key, 16-byte aligned
   __nv_bfloat16* O;
   float* residual;
   float* lse;
@@ -79,21 +97,26 @@ struct Attn1hArgs {
 };
 
 struct Attn1hSmem {
-  uint8_t q[2][kTileBytes];
-  uint8_t k[2][kTileBytes];
+  uint8_t q[kTileBytes];
+  uint8_t k[kKStages][kTileBytes];
   uint8_t v[2][kTileBytes];
+  // the epilogue's staging box for TMA stores: 128 rows x 128 bytes (64 bf16
+  // or 32 fp32 output columns), 128-byte swizzle
+  uint8_t ostage[kBQ * 128];
   uint8_t qx[kXBytes];     // ones in columns 0 and 1
-  uint8_t kx[2][kXBytes];  // per stage: the key bias as bf16 hi, lo in columns 0 and 1
-  float ls[2][kBK];
-  float ml[2][2][2][kBQ];  // [unit parity][half][max, sum][row]
-  uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
-  uint64_t ls_full[2], ls_empty[2];
+  uint8_t kx[2][kXBytes];  // per tile parity: the key bias as bf16 hi, lo in columns 0 and 1
+  float xm[2][2][kBQ];  // [half][tile parity][row]: each half's max of its 64 logits
+  float ml[2][2][kBQ];  // [unit parity][half][row]: each half's running sum
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kKStages], k_empty[kKStages];  // k_empty: that stage's Q K^T is done
   uint64_t bias_full[2];
-  uint64_t s_full[2], pa_full[2], pb_full[2], pv_done[2];
+  uint64_t v_full[2];
+  // s_full[s]: Q K^T into TMEM buffer S_s is done.  s_free[s]: both halves
+  // have loaded S_s.  p_full[s]: both halves have written P_s.  pv_done[s]:
+  // P_s V is done (P_s and V_s free, O updated).
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t o_done, o_free;
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -111,13 +134,33 @@ __device__ __forceinline__ int unit_index(const Attn1hArgs& a, int c, int k) {
   return j < a.n_units ? j : -1;
 }
 
+template <bool SPIN = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0)
+    ok = (SPIN ? mbar_wait_spin(bar, parity, abort, status) : mbar_wait(bar, parity, abort, status))
+             ? 1
+             : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&w)[4]) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
+               : "memory");
+}
+
+// ls of keys key0 .. key0 + 3 (key0 a multiple of 4; 0 past the last key).
+__device__ __forceinline__ float4 load_ls4(const float* ls, int M, int key0) {
+  if (key0 + 3 < M) return __ldg(reinterpret_cast<const float4*>(ls + key0));
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (key0 < M) v.x = __ldg(ls + key0);
+  if (key0 + 1 < M) v.y = __ldg(ls + key0 + 1);
+  if (key0 + 2 < M) v.z = __ldg(ls + key0 + 2);
+  return v;
 }
 
 __device__ __forceinline__ uint32_t split_bf16(float v) {
@@ -128,9 +171,14 @@ __device__ __forceinline__ uint32_t split_bf16(float v) {
 
 // Softmax of one half (32 x 2 = 64 key columns of every tile) for one unit,
 // then that half's share of the epilogue (64 of the 128 output columns).
-__device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& args, uint32_t tmem,
-                                             int rb, int h, uint32_t& g, int u_local, bool& ok,
-                                             int warp, int lane, volatile int* abort) {
+// The two halves of a row share one running max: per tile each half takes
+// the max of its 64 logits, the two threads of a row swap them through
+// shared memory (one 64-thread named barrier per warp pair), and both take
+// the same decision to raise it.  So both halves accumulate into one O.
+__device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& args,
+                                             const CUtensorMap& tm_out, uint32_t tmem, int rb,
+                                             int h, uint32_t& g, int u_local, bool& ok, int warp,
+                                             int lane, volatile int* abort) {
   const int half = (warp - 4) >> 2;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
@@ -139,41 +187,53 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
   const float sc = args.scale2;
   const uint64_t scale2 = f2(sc, sc);
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-  const uint32_t o_mine = tmem + 256 + half * 128 + lane_off;
+  const uint32_t o_mine = tmem + kOCol + half * 64 + lane_off;  // this half's 64 O columns
   const int nk = rb + 1;
   float m_run = -INFINITY, l_run = 0.f;
   for (int i = 0; i < nk; ++i, ++g) {
-    if (!ok) continue;
     const uint32_t st = g & 1, ph = (g >> 1) & 1;
-    if (!(ok = warp_wait(smem_u32(&S.s_full[st]), ph, abort, args.status))) continue;
-    tc_fence_after();
-    const uint32_t s_tmem = tmem + st * 128 + lane_off + col0;
+    // Every iteration reaches the pair barrier below, also after a wait gave
+    // up (then with nothing to exchange), so that the other half never
+    // waits on it in vain.
+    const bool live = ok && (ok = warp_wait(smem_u32(&S.s_full[st]), ph, abort, args.status));
     uint32_t u[2][32];
-    tmem_ld32(s_tmem, u[0]);
-    tmem_ld32(s_tmem + 32, u[1]);
-    tmem_ld_wait();
-    if (i == rb) {  // the diagonal tile: key col0 + c is row rb * 128 + col0 + c
+    float mx = -INFINITY;
+    if (live) {
+      tc_fence_after();
+      const uint32_t s_tmem = tmem + st * 128 + lane_off + col0;
+      tmem_ld32(s_tmem, u[0]);
+      tmem_ld32(s_tmem + 32, u[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.s_free[st]));  // S_st may be overwritten
+      if (i == rb) {  // the diagonal tile: key col0 + c is row rb * 128 + col0 + c
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (col0 + c > r) u[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-    }
-    float mc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      mc[k] = fmaxf(__uint_as_float(u[0][2 * k]), __uint_as_float(u[0][2 * k + 1]));
-#pragma unroll
-    for (int c = 8; c < 64; c += 8) {
+        for (int c = 0; c < 64; ++c)
+          if (col0 + c > r) u[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+      float mc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mc[k] = fmax3(mc[k], __uint_as_float(u[c >> 5][(c + 2 * k) & 31]),
-                      __uint_as_float(u[c >> 5][(c + 2 * k + 1) & 31]));
+        mc[k] = fmaxf(__uint_as_float(u[0][2 * k]), __uint_as_float(u[0][2 * k + 1]));
+#pragma unroll
+      for (int c = 8; c < 64; c += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mc[k] = fmax3(mc[k], __uint_as_float(u[c >> 5][(c + 2 * k) & 31]),
+                        __uint_as_float(u[c >> 5][(c + 2 * k + 1) & 31]));
+      }
+      mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
     }
-    const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
-    const float m_new = fmaxf(m_run, mx);
+    S.xm[half][st][r] = mx;
+    asm volatile("bar.sync %0, 64;" ::"r"(3 + quad) : "memory");  // warps 4 + quad, 8 + quad
+    const float mx_other = S.xm[half ^ 1][st][r];
+    if (!live) continue;
+    const float m_new = fmax3(m_run, mx, mx_other);
     const bool need = m_new > m_run + kRescaleThreshold;
     const float m_old = m_run;
     if (need) m_run = m_new;
-    // a half with no visible key yet (all -inf) subtracts 0, so p = 0
+    // a row with no visible key yet (all -inf) subtracts 0, so p = 0
     const float m_sub = m_run == -INFINITY ? 0.f : m_run;
     const uint64_t neg_m = f2(-m_sub, -m_sub);
     uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -190,14 +250,17 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
       acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
       pk[k] = pack_bf16x2(p0, p1);
     }
-    tmem_st32(tmem + st * 128 + lane_off + col0, pk);  // P over this half's first 32 columns
     float sum;
     {
       float a0, a1;
       f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
       sum = a0 + a1;
     }
-    // raise this half's O to the new max once the previous tile's P V is in
+    // P_st was last read by the P V two tiles back
+    if (!(ok = warp_wait(smem_u32(&S.pv_done[st]), ph ^ 1, abort, args.status))) continue;
+    tc_fence_after();
+    tmem_st32(tmem + kPCol + st * 64 + half * 32 + lane_off, pk);
+    // raise O to the new max once the previous tile's P V is in
     if (__any_sync(0xffffffffu, need) && i > 0) {
       const uint32_t pg = g - 1;
       if (!(ok = warp_wait(smem_u32(&S.pv_done[pg & 1]), (pg >> 1) & 1, abort, args.status))) {
@@ -209,7 +272,7 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
       l_run *= f;
       uint32_t w[32];
 #pragma unroll
-      for (int c0 = 0; c0 < kDH; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         tmem_ld32(o_mine + c0, w);
         tmem_ld_wait();
 #pragma unroll
@@ -221,68 +284,86 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
     l_run += sum;
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(half == 0 ? &S.pa_full[st] : &S.pb_full[st]));
+    if (lane == 0) mbar_arrive(smem_u32(&S.p_full[st]));
   }
   // ------------------------------------------------------------ epilogue
+  // O (this half's 64 columns of it) is read from TMEM into registers, then
+  // written out through the shared staging box with TMA: a bf16 output in
+  // two boxes of 64 columns (half A, then half B), an fp32 residual added
+  // element-wise by TMA in four boxes of 32 columns.  Thread-per-row stores
+  // straight from registers hit 32 rows per instruction and took ~2000
+  // cycles per unit.  One thread (warp 4, lane 0) issues the copies and
+  // waits for each to have read the box before it is refilled.
   const bool have = ok && warp_wait(smem_u32(&S.o_done), u_local & 1, abort, args.status);
   ok = have;
   if (have) tc_fence_after();
-  float* ml = &S.ml[u_local & 1][0][0][0];
-  ml[(half * 2 + 0) * kBQ + r] = m_run;
-  ml[(half * 2 + 1) * kBQ + r] = l_run;
-  asm volatile("bar.sync 2, 256;" ::: "memory");  // both halves' (max, sum) of every row
+  S.ml[u_local & 1][half][r] = l_run;
+  const bool issuer = warp == 4 && lane == 0;
+  if (issuer) bulk_wait_read_all();  // the previous unit's last box is out of the staging buffer
+  asm volatile("bar.sync 2, 256;" ::: "memory");  // both halves' sums of every row
+  const bool res = args.residual != nullptr;
+  float inv = 0.f;
   if (have) {
-    const float mA = ml[0 * kBQ + r], lA = ml[1 * kBQ + r];
-    const float mB = ml[2 * kBQ + r], lB = ml[3 * kBQ + r];
-    const float m = fmaxf(mA, mB);
-    const float fA = mA == -INFINITY ? 0.f : exp2_approx(mA - m);
-    const float fB = mB == -INFINITY ? 0.f : exp2_approx(mB - m);
-    const float inv = 1.f / (lA * fA + lB * fB);
-    const float cA = fA * inv, cB = fB * inv;
-    const bool row_ok = row < args.M;
-    if (half == 0 && args.lse != nullptr && row_ok)
-      args.lse[static_cast<int64_t>(h) * args.M + row] = (m + log2f(lA * fA + lB * fB)) * kLn2;
-    const uint32_t oa = tmem + 256 + lane_off, ob = tmem + 384 + lane_off;
-#pragma unroll 1
-    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
-      uint32_t a[32], bv[32];
-      tmem_ld32(oa + c0, a);
-      tmem_ld32(ob + c0, bv);
-      tmem_ld_wait();
-      if (row_ok) {
-        if (args.residual != nullptr) {
-          float4* dst =
-              reinterpret_cast<float4*>(args.residual + row * args.ldo + h * kDH + c0);
+    const float l = S.ml[u_local & 1][0][r] + S.ml[u_local & 1][1][r];
+    inv = 1.f / l;
+    if (half == 0 && args.lse != nullptr && row < args.M)
+      args.lse[static_cast<int64_t>(h) * args.M + row] = (m_run + log2f(l)) * kLn2;
+  }
+  const int npass = res ? 4 : 2;
+  const uint32_t stage = smem_u32(S.ostage);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4 x = dst[q];
-            x.x += __uint_as_float(a[4 * q + 0]) * cA + __uint_as_float(bv[4 * q + 0]) * cB;
-            x.y += __uint_as_float(a[4 * q + 1]) * cA + __uint_as_float(bv[4 * q + 1]) * cB;
-            x.z += __uint_as_float(a[4 * q + 2]) * cA + __uint_as_float(bv[4 * q + 2]) * cB;
-            x.w += __uint_as_float(a[4 * q + 3]) * cA + __uint_as_float(bv[4 * q + 3]) * cB;
-            dst[q] = x;
-          }
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(args.O + row * args.ldo + h * kDH + c0);
+  for (int p = 0; p < 4; ++p) {
+    if (p == npass) break;
+    if (p > 0) {
+      if (issuer) bulk_wait_read_all();
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // the staging box is free
+    }
+    const int owner = res ? (p >> 1) : p;  // the half whose columns this box holds
+    if (have && half == owner) {
+      // row r's 128 bytes: 16-byte chunk c at chunk position c ^ (r & 7)
+      const uint32_t row_base = stage + r * 128;
+      if (res) {
+        uint32_t a[32];
+        tmem_ld32(o_mine + (p & 1) * 32, a);
+        tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float o[8];
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              o[k] = __uint_as_float(a[8 * q + k]) * cA + __uint_as_float(bv[8 * q + k]) * cB;
-            uint4 w;
-            w.x = pack_bf16x2(o[0], o[1]);
-            w.y = pack_bf16x2(o[2], o[3]);
-            w.z = pack_bf16x2(o[4], o[5]);
-            w.w = pack_bf16x2(o[6], o[7]);
-            dst[q] = w;
+          for (int k = 0; k < 4; ++k) w[k] = __float_as_uint(__uint_as_float(a[4 * c + k]) * inv);
+          st_shared_v4(row_base + ((c ^ (r & 7)) << 4), w);
+        }
+      } else {
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          uint32_t a[32];
+          tmem_ld32(o_mine + hc * 32, a);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 4 * hc; c < 4 * hc + 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              w[k] = pack_bf16x2(__uint_as_float(a[(8 * c + 2 * k) & 31]) * inv,
+                                 __uint_as_float(a[(8 * c + 2 * k + 1) & 31]) * inv);
+            st_shared_v4(row_base + ((c ^ (r & 7)) << 4), w);
           }
         }
       }
+      if (!res || (p & 1)) {  // this half has read all of its O columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.o_free));  // O may be overwritten
+      }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&S.o_free));  // O may be overwritten
+    fence_proxy_async_smem();
+    asm volatile("bar.sync 2, 256;" ::: "memory");  // the box is written
+    if (issuer && have) {
+      const int x = h * kDH + owner * 64 + (res ? (p & 1) * 32 : 0);
+      if (res) tma_reduce_add_2d(&tm_out, stage, x, rb * kBQ);
+      else tma_store_2d(&tm_out, stage, x, rb * kBQ);
+      bulk_commit();
+    }
   }
 }
 
@@ -292,54 +373,45 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
 // them this way keeps every descriptor in registers (an array indexed by
 // the stage would live in local memory and slow each MMA issue).
 template <bool BIAS>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t g, uint32_t qb,
-                                         const uint64_t (&qd0)[kDH / 16], uint64_t kd0,
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t s, uint32_t ks,
+                                         const uint64_t (&qd)[kDH / 16], uint64_t kd0,
                                          uint64_t qxd, uint64_t kxd0) {
   constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);
-  const uint32_t s = g & 1;
   const uint32_t s_tmem = tmem + s * 128;
-  const uint64_t kd = kd0 + s * (kTileBytes >> 4);
-  const uint64_t qoff = qb * (kTileBytes >> 4);
+  const uint64_t kd = kd0 + ks * (kTileBytes >> 4);
 #pragma unroll
   for (int kk = 0; kk < kDH / 16; ++kk)
-    mma_ss(s_tmem, qd0[kk] + qoff, kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
+    mma_ss(s_tmem, qd[kk], kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
            kk > 0 ? 1u : 0u);
   if (BIAS) mma_ss(s_tmem, qxd, kxd0 + s * (kXBytes >> 4), idesc_s, 1u);
 }
 
-// P V of tile t (unit-local index it): both halves, into O_A and O_B.
+// P V of tile t (unit-local index it): both halves' P (64 + 64 keys) into O.
 __device__ __forceinline__ bool issue_pv(Attn1hSmem& S, const Attn1hArgs& args, uint32_t tmem,
                                          uint32_t t, int it, int u_local, uint64_t vd0,
                                          volatile int* abort) {
   constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // V MN-major
   const uint32_t st = t & 1, ph = (t >> 1) & 1;
-  if (!mbar_wait(smem_u32(&S.v_full[st]), ph, abort, args.status)) return false;
+  if (!mbar_wait_spin(smem_u32(&S.v_full[st]), ph, abort, args.status)) return false;
   if (it == 0 && u_local > 0 &&
       !mbar_wait(smem_u32(&S.o_free), (u_local - 1) & 1, abort, args.status))
     return false;
+  if (!mbar_wait(smem_u32(&S.p_full[st]), ph, abort, args.status)) return false;
+  tc_fence_after();
   const uint64_t vd = vd0 + st * (kTileBytes >> 4);
-  const uint32_t p_tmem = tmem + st * 128;
-  if (!mbar_wait(smem_u32(&S.pa_full[st]), ph, abort, args.status)) return false;
-  tc_fence_after();
+  const uint32_t p_tmem = tmem + kPCol + st * 64;
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    mma_ts(tmem + 256, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o,
-           (it > 0 || kk > 0) ? 1u : 0u);
-  if (!mbar_wait(smem_u32(&S.pb_full[st]), ph, abort, args.status)) return false;
-  tc_fence_after();
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    mma_ts(tmem + 384, p_tmem + 64 + kk * 8, vd + (4 + kk) * (2048 >> 4), idesc_o,
+  for (int kk = 0; kk < kBK / 16; ++kk)
+    mma_ts(tmem + kOCol, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o,
            (it > 0 || kk > 0) ? 1u : 0u);
   mma_commit(smem_u32(&S.pv_done[st]));
-  mma_commit(smem_u32(&S.v_empty[st]));
   return true;
 }
 
 template <bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
     keybias_attn_1h_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                           const __grid_constant__ CUtensorMap tm_ls, const Attn1hArgs args) {
+                           const __grid_constant__ CUtensorMap tm_out, const Attn1hArgs args) {
   extern __shared__ uint8_t smem_raw[];
   Attn1hSmem& S = *reinterpret_cast<Attn1hSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
@@ -348,30 +420,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &S.abort;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&S.q_full[s]), 1);
-      mbar_init(smem_u32(&S.q_empty[s]), 1);
+    mbar_init(smem_u32(&S.q_full), 1);
+    mbar_init(smem_u32(&S.q_empty), 1);
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&S.k_full[s]), 1);
       mbar_init(smem_u32(&S.k_empty[s]), 1);
-      mbar_init(smem_u32(&S.v_full[s]), 1);
-      mbar_init(smem_u32(&S.v_empty[s]), 1);
-      mbar_init(smem_u32(&S.ls_full[s]), 1);
-      mbar_init(smem_u32(&S.ls_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&S.bias_full[s]), 1);
+      mbar_init(smem_u32(&S.v_full[s]), 1);
       mbar_init(smem_u32(&S.s_full[s]), 1);
-      mbar_init(smem_u32(&S.pa_full[s]), 4);
-      mbar_init(smem_u32(&S.pb_full[s]), 4);
+      mbar_init(smem_u32(&S.s_free[s]), 8);
+      mbar_init(smem_u32(&S.p_full[s]), 8);
       mbar_init(smem_u32(&S.pv_done[s]), 1);
     }
     mbar_init(smem_u32(&S.o_done), 1);
     mbar_init(smem_u32(&S.o_free), 8);
-    mbar_init(smem_u32(&S.drain), 1);
+    mbar_init(smem_u32(&S.drain[0]), 1);
+    mbar_init(smem_u32(&S.drain[1]), 1);
     S.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_qkv);
-    if (BIAS) tma_prefetch_desc(&tm_ls);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.tmem_base), 512);
@@ -405,92 +476,107 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j < 0) break;
       int rb, h;
       unit_of(args, j, rb, h);
-      softmax_unit(S, args, tmem, rb, h, g, k, ok, warp, lane, abort);
+      softmax_unit(S, args, tm_out, tmem, rb, h, g, k, ok, warp, lane, abort);
     }
+    if (warp == 4 && lane == 0) bulk_wait_all();  // the last output box is in global memory
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 152;" ::: "memory");
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------- TMA
+      // Per tile g: K_g and ls_g, then V of the tile before (V_g is needed one
+      // tile later than K_g, and its stage frees later, after the P V two
+      // tiles back; issuing it one tile behind keeps that wait off the K
+      // fills).
       const uint64_t pol = l2_policy_evict_last();  // K/V tiles are re-read by later units
-      uint32_t g = 0;
-      int nq = 0;
+      uint32_t g = 0, nv = 0, ks = 0, kph = 0;  // tiles, V fills, K-ring stage and phase
+      int nq = 0, v_col = 0, v_row = 0;
       bool ok = true;
+      auto fill_v = [&]() -> bool {  // V of tile nv
+        const uint32_t s = nv & 1, ph = (nv >> 1) & 1;
+        if (!mbar_wait(smem_u32(&S.pv_done[s]), ph ^ 1, abort, args.status)) return false;
+        mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_2d_hint(smem_u32(S.v[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.v_full[s]),
+                           v_col + bx * 64, v_row, pol);
+        ++nv;
+        return true;
+      };
       for (int k = 0; ok; ++k) {
         const int j = unit_index(args, cta, k);
         if (j < 0) break;
         int rb, h;
         unit_of(args, j, rb, h);
         const int hk = h / args.G;
-        const uint32_t qb = k & 1;
-        if (!(ok = mbar_wait(smem_u32(&S.q_empty[qb]), ((k >> 1) & 1) ^ 1, abort, args.status)))
-          break;
-        mbar_arrive_expect_tx(smem_u32(&S.q_full[qb]), kTileBytes);
+        // Q is free once the previous unit's last Q K^T is done
+        if (!(ok = mbar_wait(smem_u32(&S.q_empty), (k & 1) ^ 1, abort, args.status))) break;
+        mbar_arrive_expect_tx(smem_u32(&S.q_full), kTileBytes);
         for (int bx = 0; bx < 2; ++bx)
-          tma_load_2d(smem_u32(S.q[qb]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full[qb]),
+          tma_load_2d(smem_u32(S.q) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.q_full),
                       h * kDH + bx * 64, rb * kBQ);
         ++nq;
         const int kcol = (args.Hq + hk) * kDH;
         for (int i = 0; i <= rb && ok; ++i, ++g) {
-          const uint32_t s = g & 1, ph = (g >> 1) & 1;
-          if (!(ok = mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status))) break;
-          mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
+          // K_g's stage is free once Q K^T of tile g - 3 is done
+          if (!(ok = mbar_wait(smem_u32(&S.k_empty[ks]), kph ^ 1, abort, args.status))) break;
+          mbar_arrive_expect_tx(smem_u32(&S.k_full[ks]), kTileBytes);
           for (int bx = 0; bx < 2; ++bx)
-            tma_load_2d_hint(smem_u32(S.k[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.k_full[s]),
-                             kcol + bx * 64, i * kBK, pol);
-          if (BIAS) {
-            if (!(ok = mbar_wait(smem_u32(&S.ls_empty[s]), ph ^ 1, abort, args.status))) break;
-            mbar_arrive_expect_tx(smem_u32(&S.ls_full[s]), kBK * 4);
-            tma_load_1d(smem_u32(S.ls[s]), &tm_ls, smem_u32(&S.ls_full[s]), i * kBK);
-          }
+            tma_load_2d_hint(smem_u32(S.k[ks]) + bx * kHalfBytes, &tm_qkv,
+                             smem_u32(&S.k_full[ks]), kcol + bx * 64, i * kBK, pol);
+          if (++ks == kKStages) ks = 0, kph ^= 1;
+          if (g > 0 && !(ok = fill_v())) break;
+          v_col = (args.Hq + args.Hkv + hk) * kDH;
+          v_row = i * kBK;
         }
       }
+      if (ok && nv < g) fill_v();  // the last tile's V
       // drain: every issued copy lands before the CTA may exit.  Each ring's
-      // last fill per stage; fills already consumed return at once.  The
-      // count g includes a fill whose wait gave up, so on that path a drain
-      // wait may give up too (bounded).
-      for (uint32_t s = 0; s < 2; ++s) {
-        if (static_cast<int>(s) < nq)
-          mbar_wait_drain(smem_u32(&S.q_full[s]), ((nq - 1 - s) >> 1) & 1);
-        if (s < g) {
-          const uint32_t last = ((g - 1 - s) >> 1) & 1;
-          mbar_wait_drain(smem_u32(&S.k_full[s]), last);
-          if (BIAS) mbar_wait_drain(smem_u32(&S.ls_full[s]), last);
-        }
+      // last fill per stage; fills already consumed return at once.  After a
+      // wait gave up the counts may miss a fill, and a drain wait may give up
+      // too (bounded).
+      if (nq > 0) mbar_wait_drain(smem_u32(&S.q_full), (nq - 1) & 1);
+      for (uint32_t s = 0; s < static_cast<uint32_t>(kKStages) && s < g; ++s) {
+        const uint32_t last = ((g - 1 - s) / kKStages) & 1;
+        mbar_wait_drain(smem_u32(&S.k_full[s]), last);
       }
-    } else if (warp == 3 && lane == 0) {
-      // ------------------------------------------------------------ TMA, V
-      // V has a producer of its own: a V fill waits for the P V two tiles
-      // back, and must not hold up the K fills behind it.
-      const uint64_t pol = l2_policy_evict_last();
-      uint32_t g = 0;
+      for (uint32_t s = 0; s < 2 && s < nv; ++s)
+        mbar_wait_drain(smem_u32(&S.v_full[s]), ((nv - 1 - s) >> 1) & 1);
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------- MMA: Q K^T
+      uint64_t qd[kDH / 16];
+#pragma unroll
+      for (int kk = 0; kk < kDH / 16; ++kk)
+        qd[kk] = smem_desc_sw128(smem_u32(S.q) + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16,
+                                 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_u32(S.k[0]), 16, 1024);
+      const uint64_t qxd = smem_desc_noswizzle(smem_u32(S.qx), kXLbo, kXSbo);
+      const uint64_t kxd0 = smem_desc_noswizzle(smem_u32(S.kx[0]), kXLbo, kXSbo);
+      uint32_t g = 0, ks = 0, kph = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int j = unit_index(args, cta, k);
         if (j < 0) break;
         int rb, h;
         unit_of(args, j, rb, h);
-        const int vcol = (args.Hq + args.Hkv + h / args.G) * kDH;
+        if (!(ok = mbar_wait_spin(smem_u32(&S.q_full), k & 1, abort, args.status))) break;
         for (int i = 0; i <= rb; ++i, ++g) {
           const uint32_t s = g & 1, ph = (g >> 1) & 1;
-          if (!(ok = mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort, args.status))) break;
-          mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
-          for (int bx = 0; bx < 2; ++bx)
-            tma_load_2d_hint(smem_u32(S.v[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.v_full[s]),
-                             vcol + bx * 64, i * kBK, pol);
+          ok = mbar_wait_spin(smem_u32(&S.k_full[ks]), kph, abort, args.status);
+          if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[s]), ph, abort, args.status);
+          // S_s is free once the softmax has loaded S of tile g - 2
+          if (ok) ok = mbar_wait(smem_u32(&S.s_free[s]), ph ^ 1, abort, args.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk<BIAS>(tmem, s, ks, qd, kd0, qxd, kxd0);
+          mma_commit(smem_u32(&S.s_full[s]));
+          mma_commit(smem_u32(&S.k_empty[ks]));
+          if (i == rb) mma_commit(smem_u32(&S.q_empty));
+          if (++ks == kKStages) ks = 0, kph ^= 1;
         }
       }
-      for (uint32_t s = 0; s < 2 && s < g; ++s)
-        mbar_wait_drain(smem_u32(&S.v_full[s]), ((g - 1 - s) >> 1) & 1);
-    } else if (warp == 1 && lane == 0) {
-      // ------------------------------------------------------------- MMA
-      uint64_t qd0[kDH / 16];
-#pragma unroll
-      for (int kk = 0; kk < kDH / 16; ++kk)
-        qd0[kk] = smem_desc_sw128(smem_u32(S.q[0]) + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16,
-                                  1024);
-      const uint64_t kd0 = smem_desc_sw128(smem_u32(S.k[0]), 16, 1024);
-      const uint64_t qxd = smem_desc_noswizzle(smem_u32(S.qx), kXLbo, kXSbo);
-      const uint64_t kxd0 = smem_desc_noswizzle(smem_u32(S.kx[0]), kXLbo, kXSbo);
+      mma_commit(smem_u32(&S.drain[0]));
+      mbar_wait_drain(smem_u32(&S.drain[0]), 0);
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------- MMA: P V
       const uint64_t vd0 = smem_desc_sw128(smem_u32(S.v[0]), kHalfBytes, 1024);
       uint32_t g = 0;
       bool ok = true;
@@ -499,29 +585,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < 0) break;
         int rb, h;
         unit_of(args, j, rb, h);
-        const uint32_t qb = k & 1;
-        if (!(ok = mbar_wait(smem_u32(&S.q_full[qb]), (k >> 1) & 1, abort, args.status))) break;
-        tc_fence_after();
-        for (int i = 0; i <= rb; ++i, ++g) {
-          const uint32_t s = g & 1, ph = (g >> 1) & 1;
-          ok = mbar_wait(smem_u32(&S.k_full[s]), ph, abort, args.status);
-          if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[s]), ph, abort, args.status);
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk<BIAS>(tmem, g, qb, qd0, kd0, qxd, kxd0);
-          mma_commit(smem_u32(&S.s_full[s]));
-          mma_commit(smem_u32(&S.k_empty[s]));
-          if (i == rb) mma_commit(smem_u32(&S.q_empty[qb]));
-          if (i > 0 && !(ok = issue_pv(S, args, tmem, g - 1, i - 1, k, vd0, abort))) break;
-        }
+        for (int i = 0; i <= rb; ++i, ++g)
+          if (!(ok = issue_pv(S, args, tmem, g, i, k, vd0, abort))) break;
         if (!ok) break;
-        if (!(ok = issue_pv(S, args, tmem, g - 1, rb, k, vd0, abort))) break;
         mma_commit(smem_u32(&S.o_done));
       }
-      mma_commit(smem_u32(&S.drain));
-      mbar_wait_drain(smem_u32(&S.drain), 0);
+      mma_commit(smem_u32(&S.drain[1]));
+      mbar_wait_drain(smem_u32(&S.drain[1]), 0);
     } else if (warp == 2 && BIAS) {
       // ------------------------------------------------------------ bias
+      // The key tile's ls values are read straight from global memory (16
+      // bytes per lane), one tile ahead: a 512-byte TMA fill queued behind
+      // the 32 KB K and V fills took 1.5-3k cycles to land.
       uint32_t g = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -530,11 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rb, h;
         unit_of(args, j, rb, h);
         const float f = args.gain[h] * args.bias_scale;
+        float4 nxt = load_ls4(args.logsig, args.M, 4 * lane);
         for (int i = 0; i <= rb; ++i, ++g) {
           const uint32_t s = g & 1, ph = (g >> 1) & 1;
-          if (!(ok = warp_wait(smem_u32(&S.ls_full[s]), ph, abort, args.status))) break;
-          if (!(ok = warp_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort, args.status))) break;
-          const float4 l = reinterpret_cast<const float4*>(S.ls[s])[lane];
+          const float4 l = nxt;
+          if (i < rb) nxt = load_ls4(args.logsig, args.M, (i + 1) * kBK + 4 * lane);
+          // kx[s] is free once Q K^T of tile g - 2 is done
+          if (!(ok = warp_wait(smem_u32(&S.s_full[s]), ph ^ 1, abort, args.status))) break;
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -542,10 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 split_bf16(f * lv[q]);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(smem_u32(&S.ls_empty[s]));
-            mbar_arrive(smem_u32(&S.bias_full[s]));
-          }
+          if (lane == 0) mbar_arrive(smem_u32(&S.bias_full[s]));
         }
       }
     }
@@ -575,45 +649,52 @@ cudaError_t launch_attn_bf16_1h(const void* QKV, int64_t M, int Hq, int Hkv, int
   a.scale2 = temperature / sqrtf(static_cast<float>(dh)) * kLog2e;
   a.bias_scale = sqrtf(static_cast<float>(dh)) / temperature;
   a.gain = gain;
+  a.logsig = logsig;
   a.O = static_cast<__nv_bfloat16*>(O);
   a.residual = residual;
   a.lse = lse;
   a.ldo = static_cast<int64_t>(Hq) * dh;
   a.status = device_status_word();
+  // the bias warp reads ls 16 bytes at a time
+  if (logsig != nullptr && (reinterpret_cast<uintptr_t>(logsig) & 15) != 0)
+    return cudaErrorInvalidValue;
   const int cols = (Hq + 2 * Hkv) * dh;
-  CUtensorMap tm_qkv, tm_ls;
+  CUtensorMap tm_qkv, tm_out;
   if (!make_tmap_2d(&tm_qkv, QKV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, M,
                     static_cast<uint64_t>(cols) * 2, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (logsig != nullptr) {
-    if (!make_tmap_1d_f32(&tm_ls, logsig, M, kBK)) return cudaErrorInvalidValue;
-  } else {
-    tm_ls = tm_qkv;  // unused
-  }
+  // the output: boxes of 128 rows x 128 bytes (64 bf16 columns of O, or 32
+  // fp32 columns of the residual, which TMA adds into)
+  const uint64_t ocols = static_cast<uint64_t>(Hq) * dh;
+  const bool ok_out =
+      residual != nullptr
+          ? make_tmap_2d(&tm_out, residual, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ocols, M, ocols * 4,
+                         32, kBQ, CU_TENSOR_MAP_SWIZZLE_128B)
+          : make_tmap_2d(&tm_out, O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ocols, M, ocols * 2, 64,
+                         kBQ, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok_out) return cudaErrorInvalidValue;
   const size_t smem = sizeof(Attn1hSmem) + 1024;
   const int grid = std::min(a.n_units, sm_count());
   auto kernel = logsig != nullptr ? keybias_attn_1h_kernel<true> : keybias_attn_1h_kernel<false>;
   cudaError_t err =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, stream, 1u, tm_qkv, tm_ls, a);
+  err = launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, stream, 1u, tm_qkv, tm_out, a);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
-// Short kept sequences (the two-head units fit in one wave of the SMs) are
-// set by their longest causal row: there the one-head units, whose key tiles
-// take about half as long, win (B300, M = 1868: 25 against 31.5 us).  Longer
-// ones are set by throughput, where a one-head CTA has to stream twice the
-// K/V bytes per MMA cycle through a 2-stage ring and waits on its loads
-// (M = 3507: 71.5 against 63.5 us; M = 8432: 304 against 256 us): there the
-// two-head kernel runs.
+// The one-head kernel reads each K/V tile once per q head, twice the bytes
+// of the two-head kernel, so it runs while K and V together stay well inside
+// L2 (48 MB).  There it is faster (B300, bias on: M = 1868: 22.8 against
+// 31.8 us; 3507: 57.5 against 60.5; 6784: 168 against 180; 8432: 251
+// against 255).  Beyond, HBM traffic decides (M = 131072, 512 MB of K and V:
+// 77 against 58 ms) and the two-head kernel runs.
 cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
                              const float* logsig, const float* gain, float temperature, void* O,
                              float* residual, float* lse, cudaStream_t stream) {
-  const int64_t n_rb = (M + kBQ - 1) / kBQ;
-  const int64_t two_head_units = n_rb * Hkv * ((Hq / Hkv) / 2);
-  if (two_head_units < static_cast<int64_t>(sm_count()))
+  const int64_t kv_bytes = 2 * M * Hkv * dh * 2;
+  if (kv_bytes <= (int64_t{48} << 20))
     return launch_attn_bf16_1h(QKV, M, Hq, Hkv, dh, logsig, gain, temperature, O, residual, lse,
                                stream);
   return launch_attn_bf16_2h(QKV, M, Hq, Hkv, dh, logsig, gain, temperature, O, residual, lse,
