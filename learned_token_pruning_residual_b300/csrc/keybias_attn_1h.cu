@@ -21,9 +21,9 @@
 //               (2 stages; 128 x 128 bf16, 128-byte swizzle; V one tile
 //               behind K);
 //   warp 1      one thread issues S_g = Q K_j^T (+ the bias block) into
-//               S[g % 2] (SS form) as soon as K_j is in and the softmax has
-//               loaded S of tile g - 2 (so Q K^T runs up to two tiles ahead
-//               of the softmax);
+//               S[g % 2] (SS form) as soon as K_j is in and P V of tile
+//               g - 2 is done (so Q K^T runs a tile ahead of the softmax,
+//               and the softmax's only waits are for S and, rarely, for O);
 //   warp 3      one thread issues O += P_g V_j (TS form, P read from TMEM)
 //               as soon as the softmax has written P_g.
 //               The thread issuing tcgen05.mma waits for the tensor pipe to
@@ -42,9 +42,10 @@
 // keeps its own partial row sum, added in the epilogue.  The max is only
 // raised when a row's max grows by more than 2^8 (log2 units); O is then
 // rescaled in TMEM (each half its 64 columns of it) after the previous
-// tile's P V has completed.  TMEM (512 columns): S_0 | S_1 | O | P_0 | P_1;
-// P has buffers of its own, so a Q K^T may overwrite S as soon as the
-// softmax has it in registers, without waiting for the P V that follows.
+// tile's P V has completed.  TMEM (512 columns): S_0 | S_1 | O | P_0 | P_1.
+// Q K^T of tile g waits for P V of tile g - 2: then S_{g%2} and P_{g%2} are
+// both free, and the softmax writes P without a wait of its own (each wait
+// or arrive on the softmax's path costs it ~100+ cycles per tile).
 #include <algorithm>
 
 #include "tg_device.cuh"
@@ -111,10 +112,10 @@ struct Attn1hSmem {
   uint64_t k_full[kKStages], k_empty[kKStages];  // k_empty: that stage's Q K^T is done
   uint64_t bias_full[2];
   uint64_t v_full[2];
-  // s_full[s]: Q K^T into TMEM buffer S_s is done.  s_free[s]: both halves
-  // have loaded S_s.  p_full[s]: both halves have written P_s.  pv_done[s]:
-  // P_s V is done (P_s and V_s free, O updated).
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  // s_full[s]: Q K^T into TMEM buffer S_s is done.  p_full[s]: both halves
+  // have written P_s (and are done with S_s).  pv_done[s]: P_s V is done
+  // (S_s, P_s and V_s free, O updated).
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_done, o_free;
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -204,9 +205,6 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
       tmem_ld32(s_tmem, u[0]);
       tmem_ld32(s_tmem + 32, u[1]);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.s_free[st]));  // S_st may be overwritten
       if (i == rb) {  // the diagonal tile: key col0 + c is row rb * 128 + col0 + c
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -256,9 +254,8 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
       f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
       sum = a0 + a1;
     }
-    // P_st was last read by the P V two tiles back
-    if (!(ok = warp_wait(smem_u32(&S.pv_done[st]), ph ^ 1, abort, args.status))) continue;
-    tc_fence_after();
+    // P_st was last read by the P V two tiles back, which was complete before
+    // Q K^T of this tile was issued (s_full implies it)
     tmem_st32(tmem + kPCol + st * 64 + half * 32 + lane_off, pk);
     // raise O to the new max once the previous tile's P V is in
     if (__any_sync(0xffffffffu, need) && i > 0) {
@@ -430,7 +427,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&S.bias_full[s]), 1);
       mbar_init(smem_u32(&S.v_full[s]), 1);
       mbar_init(smem_u32(&S.s_full[s]), 1);
-      mbar_init(smem_u32(&S.s_free[s]), 8);
       mbar_init(smem_u32(&S.p_full[s]), 8);
       mbar_init(smem_u32(&S.pv_done[s]), 1);
     }
@@ -562,8 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t s = g & 1, ph = (g >> 1) & 1;
           ok = mbar_wait_spin(smem_u32(&S.k_full[ks]), kph, abort, args.status);
           if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[s]), ph, abort, args.status);
-          // S_s is free once the softmax has loaded S of tile g - 2
-          if (ok) ok = mbar_wait(smem_u32(&S.s_free[s]), ph ^ 1, abort, args.status);
+          // P V of tile g - 2 done: the softmax has finished with S_s (it
+          // wrote P_s after loading S_s), and P_s is free again when the
+          // softmax sees S_g, so it stores P_g without waiting
+          if (ok) ok = mbar_wait(smem_u32(&S.pv_done[s]), ph ^ 1, abort, args.status);
           if (!ok) break;
           tc_fence_after();
           issue_qk<BIAS>(tmem, s, ks, qd, kd0, qxd, kxd0);
@@ -686,10 +684,10 @@ cudaError_t launch_attn_bf16_1h(const void* QKV, int64_t M, int Hq, int Hkv, int
 
 // The one-head kernel reads each K/V tile once per q head, twice the bytes
 // of the two-head kernel, so it runs while K and V together stay well inside
-// L2 (48 MB).  There it is faster (B300, bias on: M = 1868: 22.8 against
-// 31.8 us; 3507: 57.5 against 60.5; 6784: 168 against 180; 8432: 251
+// L2 (48 MB).  There it is faster (B300, bias on: M = 1868: 21.1 against
+// 31.8 us; 3507: 55.6 against 61.2; 6784: 161 against 181; 8432: 242.5
 // against 255).  Beyond, HBM traffic decides (M = 131072, 512 MB of K and V:
-// 77 against 58 ms) and the two-head kernel runs.
+// 80 against 57 ms) and the two-head kernel runs.
 cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
                              const float* logsig, const float* gain, float temperature, void* O,
                              float* residual, float* lse, cudaStream_t stream) {
