@@ -21,9 +21,8 @@
 //               (2 stages; 128 x 128 bf16, 128-byte swizzle; V one tile
 //               behind K);
 //   warp 1      one thread issues S_g = Q K_j^T (+ the bias block) into
-//               S[g % 2] (SS form) as soon as K_j is in and P V of tile
-//               g - 2 is done (so Q K^T runs a tile ahead of the softmax,
-//               and the softmax's only waits are for S and, rarely, for O);
+//               S[g % 3] (SS form) as soon as K_j is in and P V of tile
+//               g - 3 (which read P from that buffer) is done;
 //   warp 3      one thread issues O += P_g V_j (TS form, P read from TMEM)
 //               as soon as the softmax has written P_g.
 //               The thread issuing tcgen05.mma waits for the tensor pipe to
@@ -42,10 +41,13 @@
 // keeps its own partial row sum, added in the epilogue.  The max is only
 // raised when a row's max grows by more than 2^8 (log2 units); O is then
 // rescaled in TMEM (each half its 64 columns of it) after the previous
-// tile's P V has completed.  TMEM (512 columns): S_0 | S_1 | O | P_0 | P_1.
-// Q K^T of tile g waits for P V of tile g - 2: then S_{g%2} and P_{g%2} are
-// both free, and the softmax writes P without a wait of its own (each wait
-// or arrive on the softmax's path costs it ~100+ cycles per tile).
+// tile's P V has completed.  TMEM (512 columns): S_0 | S_1 | S_2 | O; each
+// half writes its P over the first 32 of its 64 columns of S_g, so P V of
+// tile g reads S_{g%3} and Q K^T of tile g + 3 waits for it.  With three S
+// buffers Q K^T runs up to two tiles ahead of the softmax, and the softmax's
+// only waits are for S (and, rarely, for O): each wait or arrive taken off
+// its path shortens every tile (B300, M = 8432: 254 us with two S buffers and
+// separate P buffers, 222 us this way).
 #include <algorithm>
 
 #include "tg_device.cuh"
@@ -67,10 +69,11 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column TMA box
 // single-buffered to make room (the next unit's Q loads once the current
 // unit's last Q K^T is done).
 constexpr int kKStages = 3;
-// TMEM columns: S_0 | S_1 (128 fp32 each) | O (128 fp32) | P_0 | P_1 (64
-// columns of bf16 pairs each: half A's 64 keys, then half B's)
-constexpr uint32_t kOCol = 256;
-constexpr uint32_t kPCol = 384;
+// TMEM columns: S_0 | S_1 | S_2 (128 fp32 each) | O (128 fp32).  Each
+// half writes its P (64 keys as 32 columns of bf16 pairs) over the first 32
+// of its own 64 columns of S_g once S_g is in its registers.
+constexpr int kSBufs = 3;  // S ring in TMEM
+constexpr uint32_t kOCol = kSBufs * 128;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -112,10 +115,10 @@ struct Attn1hSmem {
   uint64_t k_full[kKStages], k_empty[kKStages];  // k_empty: that stage's Q K^T is done
   uint64_t bias_full[2];
   uint64_t v_full[2];
-  // s_full[s]: Q K^T into TMEM buffer S_s is done.  p_full[s]: both halves
-  // have written P_s (and are done with S_s).  pv_done[s]: P_s V is done
-  // (S_s, P_s and V_s free, O updated).
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  // per TMEM buffer S_s (tile g in s = g % 3): s_full: Q K^T done;
+  // p_full: both halves have written P over S_s; pv_done: P V done (S_s
+  // free, O updated; also frees V stage g % 2)
+  uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_done, o_free;
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -192,7 +195,7 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
   const int nk = rb + 1;
   float m_run = -INFINITY, l_run = 0.f;
   for (int i = 0; i < nk; ++i, ++g) {
-    const uint32_t st = g & 1, ph = (g >> 1) & 1;
+    const uint32_t st = g % kSBufs, ph = (g / kSBufs) & 1, xp = g & 1;
     // Every iteration reaches the pair barrier below, also after a wait gave
     // up (then with nothing to exchange), so that the other half never
     // waits on it in vain.
@@ -201,7 +204,7 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
     float mx = -INFINITY;
     if (live) {
       tc_fence_after();
-      const uint32_t s_tmem = tmem + st * 128 + lane_off + col0;
+      const uint32_t s_tmem = tmem + st * 128 + lane_off + col0;  // this half's S
       tmem_ld32(s_tmem, u[0]);
       tmem_ld32(s_tmem + 32, u[1]);
       tmem_ld_wait();
@@ -223,9 +226,9 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
       }
       mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
     }
-    S.xm[half][st][r] = mx;
+    S.xm[half][xp][r] = mx;
     asm volatile("bar.sync %0, 64;" ::"r"(3 + quad) : "memory");  // warps 4 + quad, 8 + quad
-    const float mx_other = S.xm[half ^ 1][st][r];
+    const float mx_other = S.xm[half ^ 1][xp][r];
     if (!live) continue;
     const float m_new = fmax3(m_run, mx, mx_other);
     const bool need = m_new > m_run + kRescaleThreshold;
@@ -254,13 +257,13 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
       f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
       sum = a0 + a1;
     }
-    // P_st was last read by the P V two tiles back, which was complete before
-    // Q K^T of this tile was issued (s_full implies it)
-    tmem_st32(tmem + kPCol + st * 64 + half * 32 + lane_off, pk);
+    // P over the first 32 of this half's S columns (this tile's own buffer)
+    tmem_st32(tmem + st * 128 + col0 + lane_off, pk);
     // raise O to the new max once the previous tile's P V is in
     if (__any_sync(0xffffffffu, need) && i > 0) {
       const uint32_t pg = g - 1;
-      if (!(ok = warp_wait(smem_u32(&S.pv_done[pg & 1]), (pg >> 1) & 1, abort, args.status))) {
+      if (!(ok = warp_wait(smem_u32(&S.pv_done[pg % kSBufs]), (pg / kSBufs) & 1, abort,
+                           args.status))) {
         tmem_st_wait();
         continue;
       }
@@ -370,7 +373,7 @@ __device__ __forceinline__ void softmax_unit(Attn1hSmem& S, const Attn1hArgs& ar
 // them this way keeps every descriptor in registers (an array indexed by
 // the stage would live in local memory and slow each MMA issue).
 template <bool BIAS>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t s, uint32_t ks,
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t s, uint32_t ks, uint32_t xs,
                                          const uint64_t (&qd)[kDH / 16], uint64_t kd0,
                                          uint64_t qxd, uint64_t kxd0) {
   constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, 0, 0);
@@ -380,7 +383,7 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t s, uint32_t ks,
   for (int kk = 0; kk < kDH / 16; ++kk)
     mma_ss(s_tmem, qd[kk], kd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4), idesc_s,
            kk > 0 ? 1u : 0u);
-  if (BIAS) mma_ss(s_tmem, qxd, kxd0 + s * (kXBytes >> 4), idesc_s, 1u);
+  if (BIAS) mma_ss(s_tmem, qxd, kxd0 + xs * (kXBytes >> 4), idesc_s, 1u);
 }
 
 // P V of tile t (unit-local index it): both halves' P (64 + 64 keys) into O.
@@ -388,18 +391,19 @@ __device__ __forceinline__ bool issue_pv(Attn1hSmem& S, const Attn1hArgs& args, 
                                          uint32_t t, int it, int u_local, uint64_t vd0,
                                          volatile int* abort) {
   constexpr uint32_t idesc_o = idesc_bf16_f32(kBQ, kDH, 0, 1);  // V MN-major
-  const uint32_t st = t & 1, ph = (t >> 1) & 1;
-  if (!mbar_wait_spin(smem_u32(&S.v_full[st]), ph, abort, args.status)) return false;
+  const uint32_t st = t % kSBufs, ph = (t / kSBufs) & 1;
+  const uint32_t vs = t & 1;  // V ring stage
+  if (!mbar_wait_spin(smem_u32(&S.v_full[vs]), (t >> 1) & 1, abort, args.status)) return false;
   if (it == 0 && u_local > 0 &&
       !mbar_wait(smem_u32(&S.o_free), (u_local - 1) & 1, abort, args.status))
     return false;
   if (!mbar_wait(smem_u32(&S.p_full[st]), ph, abort, args.status)) return false;
   tc_fence_after();
-  const uint64_t vd = vd0 + st * (kTileBytes >> 4);
-  const uint32_t p_tmem = tmem + kPCol + st * 64;
+  const uint64_t vd = vd0 + vs * (kTileBytes >> 4);
+  const uint32_t p_tmem = tmem + st * 128;  // P_A in columns 0..31, P_B in 64..95
 #pragma unroll
   for (int kk = 0; kk < kBK / 16; ++kk)
-    mma_ts(tmem + kOCol, p_tmem + kk * 8, vd + kk * (2048 >> 4), idesc_o,
+    mma_ts(tmem + kOCol, p_tmem + (kk >> 2) * 64 + (kk & 3) * 8, vd + kk * (2048 >> 4), idesc_o,
            (it > 0 || kk > 0) ? 1u : 0u);
   mma_commit(smem_u32(&S.pv_done[st]));
   return true;
@@ -423,12 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&S.k_full[s]), 1);
       mbar_init(smem_u32(&S.k_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&S.bias_full[s]), 1);
-      mbar_init(smem_u32(&S.v_full[s]), 1);
+    for (int s = 0; s < kSBufs; ++s) {
       mbar_init(smem_u32(&S.s_full[s]), 1);
       mbar_init(smem_u32(&S.p_full[s]), 8);
       mbar_init(smem_u32(&S.pv_done[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&S.bias_full[s]), 1);
+      mbar_init(smem_u32(&S.v_full[s]), 1);
     }
     mbar_init(smem_u32(&S.o_done), 1);
     mbar_init(smem_u32(&S.o_free), 8);
@@ -488,8 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nq = 0, v_col = 0, v_row = 0;
       bool ok = true;
       auto fill_v = [&]() -> bool {  // V of tile nv
-        const uint32_t s = nv & 1, ph = (nv >> 1) & 1;
-        if (!mbar_wait(smem_u32(&S.pv_done[s]), ph ^ 1, abort, args.status)) return false;
+        const uint32_t s = nv & 1;
+        if (nv >= 2) {  // V stage s is free once P V of tile nv - 2 is done
+          const uint32_t pg = nv - 2;
+          if (!mbar_wait(smem_u32(&S.pv_done[pg % kSBufs]), (pg / kSBufs) & 1, abort, args.status))
+            return false;
+        }
         mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
         for (int bx = 0; bx < 2; ++bx)
           tma_load_2d_hint(smem_u32(S.v[s]) + bx * kHalfBytes, &tm_qkv, smem_u32(&S.v_full[s]),
@@ -555,16 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         unit_of(args, j, rb, h);
         if (!(ok = mbar_wait_spin(smem_u32(&S.q_full), k & 1, abort, args.status))) break;
         for (int i = 0; i <= rb; ++i, ++g) {
-          const uint32_t s = g & 1, ph = (g >> 1) & 1;
+          const uint32_t s = g % kSBufs, ph = (g / kSBufs) & 1;  // S buffer
+          const uint32_t xs = g & 1, xph = (g >> 1) & 1;           // bias block
           ok = mbar_wait_spin(smem_u32(&S.k_full[ks]), kph, abort, args.status);
-          if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[s]), ph, abort, args.status);
-          // P V of tile g - 2 done: the softmax has finished with S_s (it
-          // wrote P_s after loading S_s), and P_s is free again when the
-          // softmax sees S_g, so it stores P_g without waiting
+          if (ok && BIAS) ok = mbar_wait(smem_u32(&S.bias_full[xs]), xph, abort, args.status);
+          // S_s is free once P V of tile g - 3 (the P in it) is done
           if (ok) ok = mbar_wait(smem_u32(&S.pv_done[s]), ph ^ 1, abort, args.status);
           if (!ok) break;
           tc_fence_after();
-          issue_qk<BIAS>(tmem, s, ks, qd, kd0, qxd, kxd0);
+          issue_qk<BIAS>(tmem, s, ks, xs, qd, kd0, qxd, kxd0);
           mma_commit(smem_u32(&S.s_full[s]));
           mma_commit(smem_u32(&S.k_empty[ks]));
           if (i == rb) mma_commit(smem_u32(&S.q_empty));
@@ -605,11 +614,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float f = args.gain[h] * args.bias_scale;
         float4 nxt = load_ls4(args.logsig, args.M, 4 * lane);
         for (int i = 0; i <= rb; ++i, ++g) {
-          const uint32_t s = g & 1, ph = (g >> 1) & 1;
+          const uint32_t s = g & 1;
           const float4 l = nxt;
           if (i < rb) nxt = load_ls4(args.logsig, args.M, (i + 1) * kBK + 4 * lane);
           // kx[s] is free once Q K^T of tile g - 2 is done
-          if (!(ok = warp_wait(smem_u32(&S.s_full[s]), ph ^ 1, abort, args.status))) break;
+          if (g >= 2) {
+            const uint32_t pg = g - 2;
+            if (!(ok = warp_wait(smem_u32(&S.s_full[pg % kSBufs]), (pg / kSBufs) & 1, abort,
+                                 args.status)))
+              break;
+          }
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -684,10 +698,10 @@ cudaError_t launch_attn_bf16_1h(const void* QKV, int64_t M, int Hq, int Hkv, int
 
 // The one-head kernel reads each K/V tile once per q head, twice the bytes
 // of the two-head kernel, so it runs while K and V together stay well inside
-// L2 (48 MB).  There it is faster (B300, bias on: M = 1868: 21.1 against
-// 31.8 us; 3507: 55.6 against 61.2; 6784: 161 against 181; 8432: 242.5
+// L2 (48 MB).  There it is faster (B300, bias on: M = 1868: 19.8 against
+// 31.7 us; 3507: 50.7 against 61.1; 6784: 151 against 181; 8432: 222
 // against 255).  Beyond, HBM traffic decides (M = 131072, 512 MB of K and V:
-// 80 against 57 ms) and the two-head kernel runs.
+// 65 against 57 ms) and the two-head kernel runs.
 cudaError_t launch_attn_bf16(const void* QKV, int64_t M, int Hq, int Hkv, int dh,
                              const float* logsig, const float* gain, float temperature, void* O,
                              float* residual, float* lse, cudaStream_t stream) {
