@@ -58,8 +58,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     # Qwen3-1.7B shapes, N = 16384, 10% of the document kept (M = 1868)
     "qwen3_1p7b_n16k_keep10/gate_score": {"bytes_per_launch": 68190720 + 17920,
                                           "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 103552,
-                                           "source_sha": "14954bedf9497ba6"},
+    "qwen3_1p7b_n16k_keep10/select_topk": {"bytes_per_launch": 130304,
+                                           "source_sha": "60fe527eba4acb2d"},
     "qwen3_1p7b_n16k_keep10/gather_rows": {"bytes_per_launch": 7729152,
                                            "source_sha": "27ffa82b44661223"},
     "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24450304,
@@ -69,8 +69,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     # N = 131072, 6.25% of the document kept (M = 8432)
     "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537975808 + 367616,
                                              "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n128k_keep6p25/select_topk": {"bytes_per_launch": 594944,
-                                              "source_sha": "14954bedf9497ba6"},
+    "qwen3_1p7b_n128k_keep6p25/select_topk": {"bytes_per_launch": 588800,
+                                              "source_sha": "60fe527eba4acb2d"},
     "qwen3_1p7b_n128k_keep6p25/gather_rows": {"bytes_per_launch": 35035136 + 19968,
                                               "source_sha": "27ffa82b44661223"},
     "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51419648 + 20432896,

@@ -68,6 +68,8 @@ struct SelShared {
   uint32_t warp_b[kWarps];
   uint32_t seg_n[kSelectMaxCtas];    // candidates of each CTA
   uint32_t seg_off[kSelectMaxCtas];  // their offsets in the gathered list
+  uint32_t seg_at[kSelectMaxCtas];   // where they start in the workspace
+  uint32_t cand_at;                  // this CTA's reserved run
   uint32_t found_prefix, found_krem;
   uint32_t gt_base, eq_base;
   uint32_t cand_n, cand_total;
@@ -276,13 +278,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     pass = 1;
     if constexpr (CACHED) {
       // ---- candidates: the keys whose first digit is the threshold bin.
-      // Each CTA appends its own to its segment of the workspace and counts
-      // the keys above the bin; after one barrier every CTA gathers all
-      // candidates and finishes the select on them alone: the last two
-      // passes, and the (> T, == T) counts of the lower-ranked CTAs.
+      // Each CTA reserves a run of the workspace's candidate array (one
+      // atomic add; the runs are recorded, so the gather below reads them in
+      // CTA order whatever order the reservations came in), writes its
+      // candidates there and counts the keys above the bin; after one
+      // barrier every CTA gathers all candidates and finishes the select on
+      // them alone: the last two passes, and the (> T, == T) counts of the
+      // lower-ranked CTAs.  Only the total is capped, so a CTA with more
+      // than its share of the bin does not force the slow path.
       if (ok) {
-        const uint32_t capc = static_cast<uint32_t>(kSelectCandCap) / G;
-        uint32_t* seg = ws->cand + static_cast<size_t>(cta) * capc;
         // per-thread counts of candidates and of keys above the bin (packed
         // as cand + above << 16; each at most a slice), one block scan, then
         // each thread writes its candidates at its offset
@@ -293,35 +297,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t tot;
         const uint32_t incl = block_inclusive_scan(packed, S.warp_a, &tot);
+        const uint32_t nmine = tot & 0xFFFFu;
+        if (tid == 0) {
+          const uint32_t at = atomicAdd(&ws->cand_next, nmine);
+          S.cand_at = at;
+          __stcg(&ws->cand_at[cta], at);
+          __stcg(&ws->cnt[cta][0], tot >> 16);
+          __stcg(&ws->cnt[cta][1], nmine);
+        }
+        __syncthreads();
+        const uint32_t at = S.cand_at;
         uint32_t pos = (incl - packed) & 0xFFFFu;
         for (int i = tid; i < n; i += kThreads) {
           const uint32_t k = keys_smem[i];
           if ((k >> 21) == prefix) {
-            if (pos < capc) __stcg(seg + pos, k);
+            if (at + pos < static_cast<uint32_t>(kSelectCandCap)) __stcg(ws->cand + at + pos, k);
             ++pos;
           }
-        }
-        if (tid == 0) {
-          __stcg(&ws->cnt[cta][0], tot >> 16);
-          __stcg(&ws->cnt[cta][1], tot & 0xFFFFu);
         }
         ok = grid_barrier(ws, G, status, S);
       }
       if (ok) {
-        const uint32_t capc = static_cast<uint32_t>(kSelectCandCap) / G;
-        // every CTA's counts; candidate offsets; keys above the bin in the
-        // lower-ranked CTAs
+        // every CTA's counts and runs; candidate offsets; keys above the bin
+        // in the lower-ranked CTAs
         const uint32_t cn = tid < static_cast<int>(G) ? __ldcg(&ws->cnt[tid][1]) : 0u;
+        const uint32_t cat = tid < static_cast<int>(G) ? __ldcg(&ws->cand_at[tid]) : 0u;
         const uint32_t an = tid < cta ? __ldcg(&ws->cnt[tid][0]) : 0u;
         if (tid == 0) S.overflow = 0;
         __syncthreads();
-        if (cn > capc) S.overflow = 1;
+        if (cat + cn > static_cast<uint32_t>(kSelectCandCap)) S.overflow = 1;
         uint32_t total, an_tot;
         const uint32_t off = block_inclusive_scan(cn, S.warp_a, &total) - cn;
         block_inclusive_scan(an, S.warp_b, &an_tot);
         if (tid < static_cast<int>(G)) {
           S.seg_n[tid] = cn;
           S.seg_off[tid] = off;
+          S.seg_at[tid] = cat;
         }
         if (tid == 0) S.cand_total = total;
         __syncthreads();
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           constexpr int kBatch = 8;
           for (uint32_t sg = tid >> 5; sg < G; sg += kWarps) {
             const uint32_t ns = S.seg_n[sg], off = S.seg_off[sg];
-            const uint32_t* src2 = ws->cand + static_cast<size_t>(sg) * capc;
+            const uint32_t* src2 = ws->cand + S.seg_at[sg];
             for (uint32_t j0 = lane; j0 < ns; j0 += kBatch * 32) {
               uint32_t v[kBatch];
 #pragma unroll
@@ -474,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the histograms before its last barrier arrival, so after that barrier
   // (or when there was none: the trivial K) CTA 0 may clear them.
   if (cta == 0 && ok) {
+    if (tid == 0) __stcg(&ws->cand_next, 0u);  // every CTA reserved before the barrier
     if (!trivial) {
       for (int i = tid; i < 2048; i += kThreads) {
         if (!prefilled) __stcg(&ws->hist[0][i], 0u);
@@ -491,8 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Single-CTA select for short spans (up to kSelectSmallMaxKeys keys; its
-// time grows with the span, B300: 16128 keys 18 us, 32512 keys 26 us against
-// about 23 us for the multi-CTA select at any length): no grid barrier, no
+// time grows with the span, B300: 16128 keys 15.1 us, 24320 keys 19.4 us,
+// against 13.6 and 14.1 us for the multi-CTA select with 2048 keys per CTA,
+// which takes every span longer than 4096 keys): no grid barrier, no
 // global scratch beyond the gate's histogram.  All keys are loaded once (16-byte loads, every thread's
 // loads in flight together) into shared memory; the first pass's bin comes
 // from the gate's histogram when it is there; the other passes and the

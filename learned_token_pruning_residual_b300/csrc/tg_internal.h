@@ -75,7 +75,9 @@ struct SelectWorkspace {
   uint32_t cnt[kSelectMaxCtas][2];  // per-CTA counts exchanged between the CTAs
   uint32_t hdr[4];                  // {magic, N, doc_begin, doc_end} when the gate filled gate_hist
   uint32_t bar_count, bar_gen;      // grid barrier: arrivals, generation
-  uint32_t cand[kSelectCandCap];    // candidate keys, per-CTA segments; written before read
+  uint32_t cand_next;               // candidates reserved so far in this call
+  uint32_t cand_at[kSelectMaxCtas]; // where each CTA's candidates start in `cand`
+  uint32_t cand[kSelectCandCap];    // candidate keys, one reserved run per CTA; written before read
 };
 // Everything before `cand` must start at zero; `cand` needs no clearing.
 constexpr size_t kSelectZeroedBytes = offsetof(SelectWorkspace, cand);
@@ -85,7 +87,7 @@ static_assert(sizeof(SelectWorkspace) <= kSelectWorkspaceBytes, "select workspac
 // Spans up to this many keys take the single-CTA select (all keys cached in
 // shared memory, no grid barrier); longer spans the multi-CTA one, whose
 // launch uses select_grid_size(D) CTAs.
-constexpr int64_t kSelectSmallMaxKeys = 24576;
+constexpr int64_t kSelectSmallMaxKeys = 4096;
 int select_grid_size(int64_t D);
 
 // ---- launchers (argument checking happens in the ABI layer)

@@ -103,9 +103,11 @@ def test_select_nan_in_span_sets_status():
 def _ws_reset_words(ws):
     """The workspace words that must be zero before a select call: the four
     2048-word histograms, then (after 2 x 256 per-CTA count words) the
-    4-word header and the barrier's arrival counter."""
+    4-word header, the barrier's arrival counter and (after the barrier's
+    generation word) the candidate reservation counter."""
     w = ws.view(torch.int32)
-    return torch.cat([w[:4 * 2048], w[4 * 2048 + 512:4 * 2048 + 512 + 5]])
+    base = 4 * 2048 + 512
+    return torch.cat([w[:4 * 2048], w[base:base + 5], w[base + 6:base + 7]])
 
 
 def test_select_leaves_workspace_zeroed():
