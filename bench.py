@@ -65,7 +65,7 @@ NCU_TRAFFIC: dict[str, dict] = {
     "qwen3_1p7b_n16k_keep10/qkv_proj": {"bytes_per_launch": 24450304,
                                         "source_sha": "0f25d4a8caaef008"},
     "qwen3_1p7b_n16k_keep10/keybias_attn": {"bytes_per_launch": 15368192,
-                                            "source_sha": "2d4a4cb87ddb38e5"},
+                                            "source_sha": "1c005f0c3228e382"},
     # N = 131072, 6.25% of the document kept (M = 8432)
     "qwen3_1p7b_n128k_keep6p25/gate_score": {"bytes_per_launch": 537975808 + 367616,
                                              "source_sha": "0f25d4a8caaef008"},
@@ -75,8 +75,8 @@ NCU_TRAFFIC: dict[str, dict] = {
                                               "source_sha": "27ffa82b44661223"},
     "qwen3_1p7b_n128k_keep6p25/qkv_proj": {"bytes_per_launch": 51419648 + 20432896,
                                            "source_sha": "0f25d4a8caaef008"},
-    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69522560 + 6287232,
-                                               "source_sha": "2d4a4cb87ddb38e5"},
+    "qwen3_1p7b_n128k_keep6p25/keybias_attn": {"bytes_per_launch": 69526784 + 6329600,
+                                               "source_sha": "1c005f0c3228e382"},
     # the backward's bias-gradient kernel at M = 8432
     "qwen3_1p7b_n128k_keep6p25/keybias_bias_grad": {"bytes_per_launch": 137630464 + 3417344,
                                                     "source_sha": "3d91e7a27c9845f8"},

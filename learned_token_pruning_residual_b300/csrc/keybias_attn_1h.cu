@@ -12,9 +12,9 @@
 // the CTAs in snake order (round k goes 0..G-1 when k is even, G-1..0 when
 // odd), so the longest causal rows start first and the per-CTA sums of
 // tiles stay within one unit of each other.  Each CTA stays resident and
-// walks its units; the next unit's Q (double-buffered) and K/V tiles load
-// while the current unit finishes, and its first Q K^T runs during the
-// current unit's epilogue.
+// walks its units; the next unit's Q loads once the current unit's last Q
+// K^T is done and its K/V tiles stream in behind the current ones, so its
+// first Q K^T runs during the current unit's epilogue.
 //
 // Per CTA (384 threads):
 //   warp 0      TMA: Q of each unit, the K_j ring (3 stages) and V_j ring
@@ -138,14 +138,10 @@ __device__ __forceinline__ int unit_index(const Attn1hArgs& a, int c, int k) {
   return j < a.n_units ? j : -1;
 }
 
-template <bool SPIN = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0)
-    ok = (SPIN ? mbar_wait_spin(bar, parity, abort, status) : mbar_wait(bar, parity, abort, status))
-             ? 1
-             : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
