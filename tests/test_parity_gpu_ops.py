@@ -184,6 +184,46 @@ def test_gather_exact_and_logsig(mode):
     assert _status() == 0
 
 
+@pytest.mark.parametrize("dtype,d,N,M", [
+    ("bf16", 2048, 20000, 8432),   # the 128k workload's row size and kept count
+    ("bf16", 2048, 5000, 4999),    # nearly every row kept
+    ("f32", 2048, 3000, 1000),     # 8 KB rows
+    ("bf16", 8192, 1500, 700),     # 16 KB rows: several vector rounds per lane
+    ("bf16", 8, 300000, 140000),   # 16-byte rows (one lane), rows past one grid stride
+])
+def test_gather_large_rows_exact(dtype, d, N, M):
+    rng = np.random.default_rng(d + M)
+    Xf = rng.standard_normal((N, d)).astype(np.float32)
+    X = TI.f32_to_bf16_bits(Xf) if dtype == "bf16" else Xf
+    s = (rng.standard_normal(N) * 5).astype(np.float32)
+    idx = np.sort(rng.choice(N, M, replace=False)).astype(np.int32)
+    Y, ls = tg.tg_gather_rows(to_dev(X), to_dev(idx), to_dev(s))
+    Yr, lsr = O.gather_rows(X, idx, s)
+    got = bits(Y) if dtype == "bf16" else Y.cpu().numpy()
+    assert np.array_equal(got, Yr)
+    np.testing.assert_allclose(f64(ls), lsr, rtol=2e-6, atol=1e-7)
+    assert _status() == 0
+
+
+def test_gather_bad_indices_among_many_rows():
+    """Out-of-range indices at both ends, next to each other and in the
+    middle of a 3000-row gather of 4 KB rows: those rows are zero, every
+    other row exact."""
+    N, d, M = 4000, 2048, 3000
+    rng = np.random.default_rng(9)
+    X = TI.f32_to_bf16_bits(rng.standard_normal((N, d)).astype(np.float32) + 3.0)
+    idx = rng.integers(0, N, M).astype(np.int32)
+    bad = np.array([0, 17, 18, 40, 1500, 2999])
+    idx[bad] = np.array([-1, N, N + 5, -7, 1 << 30, N], dtype=np.int32)
+    Y, _ = tg.tg_gather_rows(to_dev(X), to_dev(idx))
+    assert tg.tg_get_device_status(raise_on_error=False) == 5   # TG_ERR_BAD_INDEX
+    got = bits(Y)
+    assert not got[bad].any()
+    good = np.setdiff1d(np.arange(M), bad)
+    assert np.array_equal(got[good], X[idx[good]])
+    assert _status() == 0
+
+
 def test_gather_identity_and_empty():
     X = TI.f32_to_bf16_bits(np.random.default_rng(1).standard_normal((130, 64)).astype(np.float32))
     Y, _ = tg.tg_gather_rows(to_dev(X), None)
