@@ -280,6 +280,22 @@ def test_gate_bf16(N, Hg, biases):
     assert _status() == 0
 
 
+@pytest.mark.parametrize("N,d", [(5000, 128), (70001, 128), (20000, 320)])
+def test_gate_bf16_short_k_loop(N, d):
+    """Hg = 256 with 2 or 5 K blocks per tile: the W1 fills, which trail the
+    residual's by a few K steps, cross tile boundaries (and with one tile per
+    CTA pair the whole K loop is shorter than that lag)."""
+    Hg = 256
+    rng = np.random.default_rng(N + d)
+    X = TI.f32_to_bf16_bits(rng.standard_normal((N, d)).astype(np.float32))
+    W1 = TI.f32_to_bf16_bits((rng.standard_normal((Hg, d)) / np.sqrt(d)).astype(np.float32))
+    b1 = (rng.standard_normal(Hg) * 0.1).astype(np.float32)
+    w2 = (rng.standard_normal(Hg) / np.sqrt(Hg)).astype(np.float32)
+    s = tg.tg_gate_score(to_dev(X), to_dev(W1), to_dev(b1), to_dev(w2), 0.25)
+    assert_gate_close(f64(s), O.gate_score(X, W1, b1, w2, 0.25))
+    assert _status() == 0
+
+
 def test_gate_bf16_zero_weight_closed_form():
     N, d, Hg = 333, 256, 32
     X = TI.f32_to_bf16_bits(np.random.default_rng(3).standard_normal((N, d)).astype(np.float32))
