@@ -113,8 +113,8 @@ tg_status tg_gate_score(const void* X, tg_dtype dtype, int64_t N, int32_t d,
  * finishes without a device error leaves it ready for the next call: its
  * histograms (including one a tg_gate_score put there), header and barrier
  * counter are back at zero (per-CTA counts, a barrier generation word and
- * the candidate keys of long spans carry over and need no reset), so it can be reused call after call on
- * one stream.  A tg_gate_score that filled it must be followed by a
+ * the candidate keys of long spans carry over and need no reset), so it can
+ * be reused call after call on one stream.  A tg_gate_score that filled it must be followed by a
  * tg_select_topk on the same workspace before the next tg_gate_score.
  * After TG_ERR_TIMEOUT, zero it again.  Calls that share a workspace must
  * not overlap on the GPU (use one workspace per stream).
@@ -141,9 +141,11 @@ size_t tg_select_workspace_bytes(int64_t N);
  * Limits: 0 <= doc_begin <= doc_end <= N < 2^31, 0 <= K <= doc_end -
  * doc_begin.  M == 0 launches nothing.  A NaN score inside the span sets
  * TG_ERR_NAN_SCORE in the device status word (NaN then ranks above +inf).
- * One launch of up to one CTA per SM (about 4096 keys each); the CTAs meet
- * at grid barriers in the workspace whose waits are bounded (a barrier that
- * never completes sets TG_ERR_TIMEOUT instead of hanging).
+ * One launch: a span of at most 4096 keys takes a single CTA (its keys in
+ * shared memory, no grid barrier); a longer one takes one CTA per ~2048
+ * keys, at most one per SM, and those CTAs meet at grid barriers in the
+ * workspace whose waits are bounded (a barrier that never completes sets
+ * TG_ERR_TIMEOUT instead of hanging).
  */
 tg_status tg_select_topk(const float* scores, int64_t N, int64_t doc_begin,
                          int64_t doc_end, int64_t K, int32_t* kept_idx,
